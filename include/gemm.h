@@ -1,0 +1,135 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ * The operation is the matrix product of "Learning to develop for GPU with GEMM as the
+ * example", section "Matrix product": C (M x N) = A (M x K) . B (K x N), where each
+ * element of C is the sum over k of A[i][k] * B[k][j].  That section's "generalised"
+ * form (section "Generalised matrix multiplication GEMM") also scales the product and
+ * adds a scaled accumulator; this library computes the plain product (alpha = 1,
+ * beta = 0) and OVERWRITES C.
+ *
+ * Layout: row-major throughout, with leading dimensions counted in elements:
+ *     A[i][k] = A[i*lda + k],  B[k][j] = B[k*ldb + j],  C[i][j] = C[i*ldc + j].
+ * The page's own examples are column-major; a column-major caller gets its product by
+ * swapping the operands (C^T = B^T . A^T) and passing the same pointers.
+ *
+ * Input types: fp32 (FFMA path), bf16 or fp16 (tensor-core path).  C is always fp32,
+ * accumulated in fp32.
+ *
+ * Memory ownership: A, B, C, x, col are caller-owned device pointers on the handle's
+ * device (any allocation the CUDA runtime can address from that device), except in
+ * gemm_run_host where they are host pointers.  The library never frees caller memory.
+ * The handle owns a small device status word, a split-K workspace (grown on demand,
+ * stream-ordered) and host-call staging buffers; gemm_destroy frees them.
+ *
+ * Streams: calls taking `stream` enqueue on that cudaStream_t (NULL = the legacy
+ * default stream) and return without waiting, except gemm_run_host and
+ * gemm_get_device_status, which synchronise the stream.  The returned status covers
+ * argument checks and launch errors only; errors raised later on the device (a
+ * bounded wait that ran out) are reported by gemm_get_device_status.
+ *
+ * Threads: a handle is not thread-safe.  Use one handle per host thread, or serialise
+ * calls.  Calls on one handle from different streams must not overlap in time when
+ * they use the split-K workspace (fp32 shapes with small M or few output tiles).
+ *
+ * Errors: every entry point returns a gemm_status_t (0 = success, negative = error)
+ * and writes nothing when it fails its argument checks.
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_ctx* gemm_handle_t; /* opaque, owned by the library */
+
+typedef enum {
+    GEMM_F32 = 0,  /* fp32 inputs, register-blocked FFMA kernels */
+    GEMM_BF16 = 1, /* bf16 inputs, tcgen05 tensor cores, fp32 accumulate */
+    GEMM_F16 = 2   /* fp16 inputs, tcgen05 tensor cores, fp32 accumulate */
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1,    /* null handle/pointer, negative size, ld < cols, ... */
+    GEMM_ERR_ALIGNMENT = -2,      /* bf16/fp16: base not 16-byte aligned or ld*2 % 16 != 0 */
+    GEMM_ERR_UNSUPPORTED = -3,    /* device is not sm_103, or a size beyond a kernel limit */
+    GEMM_ERR_CUDA = -4,           /* a CUDA runtime call or a launch failed */
+    GEMM_ERR_DEVICE_TIMEOUT = -5  /* a kernel's bounded wait ran out (see gemm_get_device_status) */
+} gemm_status_t;
+
+/* Create a handle bound to CUDA device `device`.  Queries the SM count, allocates the
+ * device status word.  The caller's current device is restored before returning.
+ * Fails with GEMM_ERR_UNSUPPORTED unless the device is compute capability 10.3. */
+int gemm_create(gemm_handle_t* out, int device);
+
+/* Destroy a handle and free the memory it owns (not caller memory).  The handle's
+ * streams must be idle (the call synchronises the device).  NULL is a no-op. */
+int gemm_destroy(gemm_handle_t h);
+
+/* C = A . B (alpha = 1, beta = 0; C is overwritten, never read).
+ *   M, N, K  >= 0.  M == 0 or N == 0: nothing is done.  K == 0: C is set to zero.
+ *   lda >= K, ldb >= N, ldc >= N (elements).  Rows may be padded; padding is never
+ *   read or written.
+ *   dtype GEMM_F32: A, B are float*; any alignment (16-byte aligned bases and ld % 4
+ *   == 0 take the vectorised loads).
+ *   dtype GEMM_BF16 / GEMM_F16: A, B are 16-bit; A, B must be 16-byte aligned and
+ *   lda, ldb multiples of 8 elements (TMA tensor-map rules), else GEMM_ERR_ALIGNMENT.
+ *   C (float*) needs no alignment beyond 4 bytes.
+ *   stream: cudaStream_t (NULL = legacy default stream).  Asynchronous.
+ * Kernel choice is by shape and dtype among this library's own kernels only. */
+int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+             const void* A, int64_t lda, const void* B, int64_t ldb,
+             float* C, int64_t ldc, gemm_dtype_t dtype, void* stream);
+
+/* The same product with A, B and C in HOST memory (pageable or pinned).  Copies A and
+ * B into handle-owned device buffers on `stream`, runs gemm_run, copies C back and
+ * synchronises `stream` before returning.  Leading dimensions as in gemm_run. */
+int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                  const void* A, int64_t lda, const void* B, int64_t ldb,
+                  float* C, int64_t ldc, gemm_dtype_t dtype, void* stream);
+
+/* Lowering of a valid (no padding, stride 1, dilation 1) 4-D cross-correlation to a
+ * GEMM operand, as in "Three X: large convolutions in PyTorch for training", section
+ * "CuBLAS" (im2col / vol2col, extended by one spatial dimension):
+ *   x   : fp32 [C_in][in[0]][in[1]][in[2]][in[3]], contiguous, device memory.
+ *   col : fp32 [C_in*k0*k1*k2*k3][P0*P1*P2*P3], contiguous, device memory, where
+ *         Pd = in[d] - k[d] + 1.  Row (c, r0, r1, r2, r3) row-major; column = output
+ *         position (p0, p1, p2, p3) row-major.
+ *         col[row][col] = x[c][p0+r0][p1+r1][p2+r2][p3+r3].
+ * With weights W as the row-major [C_out][C_in*k0*k1*k2*k3] matrix, gemm_run(W, col)
+ * gives the output [C_out][P0*P1*P2*P3].  Asynchronous on `stream`.
+ * GEMM_ERR_INVALID_ARG if any extent is <= 0 or k[d] > in[d]. */
+int conv4d_im2col(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4],
+                  const int64_t k_dims[4], float* col, void* stream);
+
+/* Synchronise `stream`, then read and clear the handle's device status word.
+ * Returns GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a kernel launched through this
+ * handle gave up on a bounded wait since the last call (its output is then invalid),
+ * or GEMM_ERR_CUDA if the stream reports an error. */
+int gemm_get_device_status(gemm_handle_t h, void* stream);
+
+/* Tuning and test options (see GEMM_OPT_*).  Values outside the documented range are
+ * rejected with GEMM_ERR_INVALID_ARG.  Defaults are restored by passing 0. */
+typedef enum {
+    GEMM_OPT_F32_KERNEL = 1, /* 0 auto, 1 tiled 128x128 FFMA, 2 tiled 64x128 FFMA, 3 skinny streaming (M<=32) */
+    GEMM_OPT_SPLIT_K = 2,    /* 0 auto, else the split-K factor for fp32 kernels (1..1024) */
+    GEMM_OPT_WAIT_LIMIT_US = 3 /* 0 default (2 s), else the bounded-wait limit of device waits in microseconds */
+} gemm_option_t;
+int gemm_set_option(gemm_handle_t h, int option, int64_t value);
+
+/* Number of kernels launched through this handle since it was created (a cumulative
+ * count kept on the host; -1 for a NULL handle).  Zero-size calls launch nothing. */
+int64_t gemm_launch_count(gemm_handle_t h);
+
+/* Static string describing a status code. */
+const char* gemm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

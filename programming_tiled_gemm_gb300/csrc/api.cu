@@ -1,0 +1,289 @@
+// Host side of the C ABI declared in include/gemm.h: handle, argument checks, kernel
+// choice among this library's own kernels, workspace and staging buffers.
+//
+// The shape of the interface follows the host pipeline of "Learning to develop for GPU
+// with GEMM as the example", section "Writing a GPU implementation of matrix
+// multiplication" (set up device buffers once, pass (m, n, k, a, b, c) to the kernel,
+// enqueue it on a queue, wait on an event): here a handle is created once, gemm_run
+// enqueues on the caller's CUDA stream, and the caller synchronises as it wishes.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+
+using namespace gemm_gb300;
+
+struct gemm_ctx {
+    int device = 0;
+    int num_sms = 0;
+    int* d_status = nullptr;  // device status word written by kernels with bounded waits
+    float* workspace = nullptr;
+    size_t workspace_bytes = 0;
+    void* stage[3] = {nullptr, nullptr, nullptr};  // gemm_run_host device copies of A, B, C
+    size_t stage_bytes[3] = {0, 0, 0};
+    int opt_f32_kernel = 0;
+    int opt_split_k = 0;
+    uint64_t wait_limit_ns = 2000000000ull;
+    int64_t launches = 0;  // kernels launched through this handle
+};
+
+namespace {
+
+class DeviceGuard {
+  public:
+    explicit DeviceGuard(int dev) : ok_(false), prev_(-1)
+    {
+        if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+        ok_ = (prev_ == dev) || (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard()
+    {
+        if (prev_ >= 0) cudaSetDevice(prev_);
+    }
+    bool ok() const { return ok_; }
+
+  private:
+    bool ok_;
+    int prev_;
+};
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA; }
+
+// Grow a device buffer to at least `bytes` (contents are not kept).
+int ensure_buffer(void** buf, size_t* have, size_t bytes)
+{
+    if (*have >= bytes && *buf) return GEMM_OK;
+    if (*buf) {
+        cudaFree(*buf);  // implicit device synchronisation: no kernel still uses it
+        *buf = nullptr;
+        *have = 0;
+    }
+    size_t want = bytes < 256 ? 256 : bytes;
+    if (cudaMalloc(buf, want) != cudaSuccess) {
+        *buf = nullptr;
+        return GEMM_ERR_CUDA;
+    }
+    *have = want;
+    return GEMM_OK;
+}
+
+int check_common(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                 const void* B, int64_t ldb, const float* C, int64_t ldc, int dtype)
+{
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_F32 && dtype != GEMM_BF16 && dtype != GEMM_F16) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (!A || !B) return GEMM_ERR_INVALID_ARG;
+        if (lda < K || ldb < N) return GEMM_ERR_INVALID_ARG;
+    }
+    // the largest element offsets must fit in int64 (they always do for real memory,
+    // but reject nonsense before it reaches a kernel)
+    const int64_t lim = (int64_t)1 << 46;
+    if (M > lim / (ldc > 0 ? ldc : 1) || (K > 0 && (M > lim / lda || K > lim / ldb)))
+        return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)
+{
+    int kernel = h->opt_f32_kernel;
+    if (kernel == 0) kernel = (a.M <= 32) ? 3 : (a.M <= 64 ? 2 : 1);
+    if (kernel == 3 && a.M > 32) return GEMM_ERR_UNSUPPORTED;
+    int split = h->opt_split_k;
+    if (split == 0)
+        split = (kernel == 3) ? skinny_auto_split(a, h->num_sms) : ffma_auto_split(a, kernel, h->num_sms);
+    if ((int64_t)split > a.K) split = (int)(a.K > 0 ? a.K : 1);
+    if (split > 1) {
+        const size_t need = (size_t)split * (size_t)a.M * (size_t)a.N * sizeof(float);
+        int rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, need);
+        if (rc != GEMM_OK) return rc;
+    }
+    cudaError_t e;
+    int n = 0;
+    if (kernel == 3)
+        e = launch_skinny(a, split, h->workspace, h->num_sms, stream, &n);
+    else
+        e = launch_ffma_tiled(a, kernel, split, h->workspace, h->num_sms, stream, &n);
+    h->launches += n;
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_create(gemm_handle_t* out, int device)
+{
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (device < 0 || device >= count) return GEMM_ERR_INVALID_ARG;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;  // kernels are built for sm_103a only
+    DeviceGuard g(device);
+    if (!g.ok()) return GEMM_ERR_CUDA;
+    gemm_ctx* h = new (std::nothrow) gemm_ctx();
+    if (!h) return GEMM_ERR_CUDA;
+    h->device = device;
+    h->num_sms = sms;
+    if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess ||
+        cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
+        if (h->d_status) cudaFree(h->d_status);
+        delete h;
+        return GEMM_ERR_CUDA;
+    }
+    *out = h;
+    return GEMM_OK;
+}
+
+int gemm_destroy(gemm_handle_t h)
+{
+    if (!h) return GEMM_OK;
+    DeviceGuard g(h->device);
+    cudaDeviceSynchronize();
+    if (h->d_status) cudaFree(h->d_status);
+    if (h->workspace) cudaFree(h->workspace);
+    for (int i = 0; i < 3; ++i)
+        if (h->stage[i]) cudaFree(h->stage[i]);
+    delete h;
+    return GEMM_OK;
+}
+
+int gemm_set_option(gemm_handle_t h, int option, int64_t value)
+{
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    switch (option) {
+    case GEMM_OPT_F32_KERNEL:
+        if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
+        h->opt_f32_kernel = (int)value;
+        return GEMM_OK;
+    case GEMM_OPT_SPLIT_K:
+        if (value < 0 || value > 1024) return GEMM_ERR_INVALID_ARG;
+        h->opt_split_k = (int)value;
+        return GEMM_OK;
+    case GEMM_OPT_WAIT_LIMIT_US:
+        if (value < 0 || value > 60000000) return GEMM_ERR_INVALID_ARG;
+        h->wait_limit_ns = value == 0 ? 2000000000ull : (uint64_t)value * 1000ull;
+        return GEMM_OK;
+    default:
+        return GEMM_ERR_INVALID_ARG;
+    }
+}
+
+int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+             const void* B, int64_t ldb, float* C, int64_t ldc, gemm_dtype_t dtype, void* stream)
+{
+    int rc = check_common(h, M, N, K, A, lda, B, ldb, C, ldc, (int)dtype);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype != GEMM_F32 && K > 0) {
+        // TMA tensor maps: 16-byte aligned bases, row strides a multiple of 16 bytes.
+        if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) || (lda % 8) ||
+            (ldb % 8))
+            return GEMM_ERR_ALIGNMENT;
+        if ((reinterpret_cast<uintptr_t>(C) & 3)) return GEMM_ERR_ALIGNMENT;
+    }
+    DeviceGuard g(h->device);
+    if (!g.ok()) return GEMM_ERR_CUDA;
+    if (K == 0) return from_cuda(cudaMemset2DAsync(C, (size_t)ldc * 4, 0, (size_t)N * 4, (size_t)M, s));
+    if (dtype == GEMM_F32) {
+        F32Args a{M, N, K, static_cast<const float*>(A), lda, static_cast<const float*>(B), ldb, C, ldc};
+        return run_f32(h, a, s);
+    }
+    TcArgs t{M, N, K, A, lda, B, ldb, C, ldc, dtype == GEMM_BF16 ? 1 : 0};
+    int n = 0;
+    int rc2 = launch_tc_gemm(t, h->num_sms, h->d_status, h->wait_limit_ns, s, &n);
+    h->launches += n;
+    return rc2;
+}
+
+int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                  const void* B, int64_t ldb, float* C, int64_t ldc, gemm_dtype_t dtype, void* stream)
+{
+    int rc = check_common(h, M, N, K, A, lda, B, ldb, C, ldc, (int)dtype);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DeviceGuard g(h->device);
+    if (!g.ok()) return GEMM_ERR_CUDA;
+    const size_t es = (dtype == GEMM_F32) ? 4 : 2;
+    // device leading dimensions: multiples of 8 elements keep every row 16-byte aligned
+    const int64_t lda_d = (K + 7) / 8 * 8, ldb_d = (N + 7) / 8 * 8, ldc_d = (N + 3) / 4 * 4;
+    if (K > 0) {
+        if ((rc = ensure_buffer(&h->stage[0], &h->stage_bytes[0], (size_t)M * lda_d * es)) != GEMM_OK) return rc;
+        if ((rc = ensure_buffer(&h->stage[1], &h->stage_bytes[1], (size_t)K * ldb_d * es)) != GEMM_OK) return rc;
+    }
+    if ((rc = ensure_buffer(&h->stage[2], &h->stage_bytes[2], (size_t)M * ldc_d * 4)) != GEMM_OK) return rc;
+    if (K > 0) {
+        if (cudaMemcpy2DAsync(h->stage[0], lda_d * es, A, lda * es, K * es, M, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess ||
+            cudaMemcpy2DAsync(h->stage[1], ldb_d * es, B, ldb * es, N * es, K, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    rc = gemm_run(h, M, N, K, h->stage[0], lda_d, h->stage[1], ldb_d, static_cast<float*>(h->stage[2]), ldc_d,
+                  dtype, stream);
+    if (rc != GEMM_OK) return rc;
+    if (cudaMemcpy2DAsync(C, ldc * 4, h->stage[2], ldc_d * 4, N * 4, M, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return from_cuda(cudaStreamSynchronize(s));
+}
+
+int conv4d_im2col(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4],
+                  const int64_t k_dims[4], float* col, void* stream)
+{
+    if (!h || !x || !col || !in_dims || !k_dims || C_in <= 0) return GEMM_ERR_INVALID_ARG;
+    for (int d = 0; d < 4; ++d)
+        if (in_dims[d] <= 0 || k_dims[d] <= 0 || k_dims[d] > in_dims[d] || in_dims[d] > (1 << 20))
+            return GEMM_ERR_INVALID_ARG;
+    if (C_in > (1 << 20)) return GEMM_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok()) return GEMM_ERR_CUDA;
+    cudaError_t e = launch_im2col4d(x, C_in, in_dims, k_dims, col, h->num_sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) h->launches += 1;
+    return from_cuda(e);
+}
+
+int64_t gemm_launch_count(gemm_handle_t h)
+{
+    return h ? h->launches : -1;
+}
+
+int gemm_get_device_status(gemm_handle_t h, void* stream)
+{
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok()) return GEMM_ERR_CUDA;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GEMM_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (v != 0) {
+        if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+        return GEMM_ERR_DEVICE_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+const char* gemm_status_string(int status)
+{
+    switch (status) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_ALIGNMENT: return "misaligned pointer or leading dimension (16-bit inputs need 16-byte alignment)";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported device or size";
+    case GEMM_ERR_CUDA: return "CUDA runtime error";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait; its output is invalid";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

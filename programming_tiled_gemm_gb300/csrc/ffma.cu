@@ -1,0 +1,292 @@
+// fp32 GEMM on the FP32 pipe: a register-blocked FFMA kernel with shared-memory tiles.
+//
+// Design (from "Learning to develop for GPU with GEMM as the example"):
+//  * section "Making the GPU implementation better": the K loop is split into tiles that
+//    are first staged in shared memory by the whole block, then multiplied;
+//  * section "How loading into local memory is organised": each thread copies its part of
+//    the tile, a barrier separates copying from use;
+//  * section "Why does tiling work?": neighbouring threads read neighbouring addresses
+//    (128-byte transactions) -- here every global access is a float4;
+//  * section "Improving the solution and balancing memory work": every thread owns a 2-D
+//    block of accumulators (TM x TN, the page's WPTM x WPTN = 8 x 8) and runs an outer
+//    product per k from registers: one A value times a row of B values, no shuffles;
+//  * section "How to do even better": rectangular tiles, A stored transposed (k-major)
+//    in shared memory, rows padded against bank conflicts.
+// What differs from the page: the tile is 128 x 128 x 8 (or 64 x 128 x 16) for 256
+// threads, global loads for tile t+1 are in flight while tile t is multiplied (two
+// shared buffers, one barrier per tile), M/N/K tails are predicated (zero fill), and an
+// optional split of K over grid.z with a fixed-order reduction fills the GPU when there
+// are few output tiles.
+#include "internal.h"
+
+namespace gemm_gb300 {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kGroupM = 8;  // output-tile rows per raster group (L2 reuse of B columns)
+
+template <int BM, int BN, int BK, int TM, int TN, bool VEC>
+__global__ void __launch_bounds__(kThreads, 2)
+ffma_tiled_kernel(F32Args p, int64_t k_per_split, int m_tiles, int n_tiles, float* ws,
+                  int vec_out)
+{
+    constexpr int TY = BM / TM;  // thread rows
+    constexpr int TX = BN / TN;  // thread columns
+    static_assert(TY * TX == kThreads, "tile/thread mismatch");
+    static_assert(TM % 4 == 0 && TN % 4 == 0 && BK % 4 == 0, "float4 fragments");
+    constexpr int AS_LD = BM + 4;  // padded row of the k-major A tile
+    constexpr int A_CNT = BM * BK / 4, B_CNT = BN * BK / 4;  // float4s per tile
+    constexpr int A_IT = (A_CNT + kThreads - 1) / kThreads;
+    constexpr int B_IT = (B_CNT + kThreads - 1) / kThreads;
+
+    __shared__ __align__(16) float As[2][BK][AS_LD];
+    __shared__ __align__(16) float Bs[2][BK][BN];
+
+    const int tid = threadIdx.x;
+
+    // Grouped raster: kGroupM consecutive tile rows sweep the tile columns together.
+    const int pid = blockIdx.x;
+    const int width = kGroupM * n_tiles;
+    const int group = pid / width;
+    const int first_m = group * kGroupM;
+    const int gsize = min(m_tiles - first_m, kGroupM);
+    const int mt = first_m + (pid % width) % gsize;
+    const int nt = (pid % width) / gsize;
+    const int64_t m0 = (int64_t)mt * BM, n0 = (int64_t)nt * BN;
+
+    const int64_t kbeg = (int64_t)blockIdx.z * k_per_split;
+    const int64_t kend = min(p.K, kbeg + k_per_split);
+
+    float* out;
+    int64_t ldo;
+    if (gridDim.z > 1) {
+        out = ws + (int64_t)blockIdx.z * p.M * p.N;
+        ldo = p.N;
+    } else {
+        out = p.C;
+        ldo = p.ldc;
+    }
+
+    float4 a_st[A_IT], b_st[B_IT];
+
+    auto load_tiles = [&](int64_t k0) {
+#pragma unroll
+        for (int i = 0; i < A_IT; ++i) {
+            const int f = tid + i * kThreads;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (f < A_CNT) {
+                const int row = f / (BK / 4);
+                const int kq = (f % (BK / 4)) * 4;
+                const int64_t gm = m0 + row, gk = k0 + kq;
+                if (gm < p.M) {
+                    const float* src = p.A + gm * p.lda + gk;
+                    if (VEC && gk + 3 < kend) {
+                        v = __ldg(reinterpret_cast<const float4*>(src));
+                    } else {
+                        if (gk + 0 < kend) v.x = __ldg(src + 0);
+                        if (gk + 1 < kend) v.y = __ldg(src + 1);
+                        if (gk + 2 < kend) v.z = __ldg(src + 2);
+                        if (gk + 3 < kend) v.w = __ldg(src + 3);
+                    }
+                }
+            }
+            a_st[i] = v;
+        }
+#pragma unroll
+        for (int i = 0; i < B_IT; ++i) {
+            const int f = tid + i * kThreads;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (f < B_CNT) {
+                const int krow = f / (BN / 4);
+                const int nq = (f % (BN / 4)) * 4;
+                const int64_t gk = k0 + krow, gn = n0 + nq;
+                if (gk < kend) {
+                    const float* src = p.B + gk * p.ldb + gn;
+                    if (VEC && gn + 3 < p.N) {
+                        v = __ldg(reinterpret_cast<const float4*>(src));
+                    } else {
+                        if (gn + 0 < p.N) v.x = __ldg(src + 0);
+                        if (gn + 1 < p.N) v.y = __ldg(src + 1);
+                        if (gn + 2 < p.N) v.z = __ldg(src + 2);
+                        if (gn + 3 < p.N) v.w = __ldg(src + 3);
+                    }
+                }
+            }
+            b_st[i] = v;
+        }
+    };
+
+    auto store_tiles = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < A_IT; ++i) {
+            const int f = tid + i * kThreads;
+            if (f < A_CNT) {
+                const int row = f / (BK / 4);
+                const int kq = (f % (BK / 4)) * 4;
+                As[buf][kq + 0][row] = a_st[i].x;  // transposed: A tile stored k-major
+                As[buf][kq + 1][row] = a_st[i].y;
+                As[buf][kq + 2][row] = a_st[i].z;
+                As[buf][kq + 3][row] = a_st[i].w;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < B_IT; ++i) {
+            const int f = tid + i * kThreads;
+            if (f < B_CNT) {
+                const int krow = f / (BN / 4);
+                const int nq = (f % (BN / 4)) * 4;
+                *reinterpret_cast<float4*>(&Bs[buf][krow][nq]) = b_st[i];
+            }
+        }
+    };
+
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+    const int ty = tid / TX, tx = tid % TX;
+    const int64_t ktiles = (kend > kbeg) ? (kend - kbeg + BK - 1) / BK : 0;
+
+    if (ktiles > 0) {
+        load_tiles(kbeg);
+        store_tiles(0);
+        __syncthreads();
+    }
+    for (int64_t kt = 0; kt < ktiles; ++kt) {
+        const int buf = (int)(kt & 1);
+        if (kt + 1 < ktiles) load_tiles(kbeg + (kt + 1) * BK);  // in flight during the FFMAs
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
+            float af[TM], bf[TN];
+#pragma unroll
+            for (int a = 0; a < TM / 4; ++a) {
+                const float4 t = *reinterpret_cast<const float4*>(&As[buf][k][ty * 4 + a * TY * 4]);
+                af[a * 4 + 0] = t.x;
+                af[a * 4 + 1] = t.y;
+                af[a * 4 + 2] = t.z;
+                af[a * 4 + 3] = t.w;
+            }
+#pragma unroll
+            for (int b = 0; b < TN / 4; ++b) {
+                const float4 t = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4 + b * TX * 4]);
+                bf[b * 4 + 0] = t.x;
+                bf[b * 4 + 1] = t.y;
+                bf[b * 4 + 2] = t.z;
+                bf[b * 4 + 3] = t.w;
+            }
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(af[i], bf[j], acc[i][j]);
+        }
+        if (kt + 1 < ktiles) store_tiles(buf ^ 1);
+        __syncthreads();
+    }
+
+    // Epilogue: each thread writes its (TM/4) x (TN/4) blocks of 4 x 4 as float4 rows.
+#pragma unroll
+    for (int a = 0; a < TM / 4; ++a) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t gm = m0 + ty * 4 + a * TY * 4 + i;
+            if (gm >= p.M) continue;
+            float* row = out + gm * ldo;
+#pragma unroll
+            for (int b = 0; b < TN / 4; ++b) {
+                const int64_t gn = n0 + tx * 4 + b * TX * 4;
+                const float* v = &acc[a * 4 + i][b * 4];
+                if (vec_out && gn + 3 < p.N) {
+                    *reinterpret_cast<float4*>(row + gn) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (gn + j < p.N) row[gn + j] = v[j];
+                }
+            }
+        }
+    }
+}
+
+// Fixed-order sum of split-K partials: C[m][n] = ws[0][m][n] + ws[1][m][n] + ...
+__global__ void __launch_bounds__(256)
+splitk_reduce_kernel(const float* __restrict__ ws, int split, int64_t M, int64_t N,
+                     float* __restrict__ C, int64_t ldc)
+{
+    const int64_t total = M * N;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        const int64_t m = idx / N, n = idx - m * N;
+        float s = ws[idx];
+        for (int z = 1; z < split; ++z) s += ws[(int64_t)z * total + idx];
+        C[m * ldc + n] = s;
+    }
+}
+
+template <int BM, int BN, int BK, int TM, int TN>
+cudaError_t launch_variant(const F32Args& a, int split, float* ws, cudaStream_t stream, int* launches)
+{
+    const int64_t m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + BN - 1) / BN;
+    if (m_tiles * n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    int64_t kps = (a.K + split - 1) / split;
+    kps = (kps + BK - 1) / BK * BK;  // every split but the last starts on a tile boundary
+    const int nsplit = (int)((a.K + kps - 1) / kps);
+    const bool vec_in = ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15) == 0 &&
+                        a.lda % 4 == 0 && a.ldb % 4 == 0;
+    int vec_out;
+    if (nsplit > 1)
+        vec_out = (a.N % 4 == 0);
+    else
+        vec_out = (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0;
+    dim3 grid((unsigned)(m_tiles * n_tiles), 1, (unsigned)nsplit);
+    if (vec_in)
+        ffma_tiled_kernel<BM, BN, BK, TM, TN, true><<<grid, kThreads, 0, stream>>>(
+            a, kps, (int)m_tiles, (int)n_tiles, ws, vec_out);
+    else
+        ffma_tiled_kernel<BM, BN, BK, TM, TN, false><<<grid, kThreads, 0, stream>>>(
+            a, kps, (int)m_tiles, (int)n_tiles, ws, vec_out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+    if (nsplit == 1) return e;
+    *launches += 1;
+    return launch_splitk_reduce(ws, nsplit, a.M, a.N, a.C, a.ldc, 0, stream);
+}
+
+}  // namespace
+
+int ffma_auto_split(const F32Args& a, int variant, int num_sms)
+{
+    const int BM = (variant == 2) ? 64 : 128, BN = 128, BK = (variant == 2) ? 16 : 8;
+    const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+    const int64_t capacity = (int64_t)num_sms * 2;  // two resident blocks per SM
+    if (tiles >= capacity) return 1;
+    int64_t s = capacity / tiles;
+    const int64_t max_s = a.K / (BK * 16);  // keep at least 16 K tiles per split
+    if (s > max_s) s = max_s;
+    return (int)(s < 1 ? 1 : s);
+}
+
+cudaError_t launch_ffma_tiled(const F32Args& a, int variant, int split, float* ws, int num_sms,
+                              cudaStream_t stream, int* launches)
+{
+    (void)num_sms;
+    if (split < 1) split = 1;
+    if (variant == 2) return launch_variant<64, 128, 16, 4, 8>(a, split, ws, stream, launches);
+    return launch_variant<128, 128, 8, 8, 8>(a, split, ws, stream, launches);
+}
+
+cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t N, float* C,
+                                 int64_t ldc, int num_sms, cudaStream_t stream)
+{
+    const int64_t total = M * N;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 152) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(ws, split, M, N, C, ldc);
+    return cudaGetLastError();
+}
+
+}  // namespace gemm_gb300

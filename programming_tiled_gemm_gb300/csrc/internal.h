@@ -1,0 +1,69 @@
+// Internal declarations shared by the library's translation units (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gemm.h"
+
+namespace gemm_gb300 {
+
+// Device status word values written by kernels (0 = no error).
+enum DeviceStatus : int {
+    kDevOk = 0,
+    kDevTimeoutProducer = 1,  // producer gave up waiting for a free pipeline stage
+    kDevTimeoutMma = 2,       // MMA issuer gave up waiting for a full stage / free accumulator
+    kDevTimeoutEpilogue = 3,  // epilogue gave up waiting for a finished accumulator
+    kDevTimeoutDrain = 4      // a CTA gave up draining its own copies / MMAs before exit
+};
+
+struct F32Args {
+    int64_t M, N, K;
+    const float* A;
+    int64_t lda;
+    const float* B;
+    int64_t ldb;
+    float* C;
+    int64_t ldc;
+};
+
+// fp32 tiled FFMA GEMM (128x128 or 32x128 block tiles), optional split-K.
+// With split > 1 the partial products go to `workspace` ([split][M][N], ld = N) and a
+// fixed-order reduction writes C.  Returns a cudaError_t.
+cudaError_t launch_ffma_tiled(const F32Args& a, int variant, int split, float* workspace,
+                              int num_sms, cudaStream_t stream, int* launches);
+
+// fp32 skinny streaming GEMM for M <= 32: B is read once, straight into registers.
+cudaError_t launch_skinny(const F32Args& a, int split, float* workspace, int num_sms,
+                          cudaStream_t stream, int* launches);
+
+// Fixed-order split-K reduction: C[m][n] = sum_{s=0..split-1} ws[s][m][n].
+cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t N, float* C,
+                                 int64_t ldc, int num_sms, cudaStream_t stream);
+
+// Every launcher adds the number of kernels it launched to *launches.
+
+// Split factors the launchers would pick on their own (0 in the option = auto).
+int ffma_auto_split(const F32Args& a, int variant, int num_sms);
+int skinny_auto_split(const F32Args& a, int num_sms);
+
+// 4-D valid cross-correlation lowering (im2col).
+cudaError_t launch_im2col4d(const float* x, int64_t cin, const int64_t in[4], const int64_t k[4],
+                            float* col, int num_sms, cudaStream_t stream);
+
+// bf16 / fp16 tensor-core GEMM (tcgen05 + TMA + TMEM), persistent.
+struct TcArgs {
+    int64_t M, N, K;
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    float* C;
+    int64_t ldc;
+    int is_bf16;  // 1 = bf16, 0 = fp16
+};
+// Returns GEMM_OK or a negative gemm_status_t.
+int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_limit_ns,
+                   cudaStream_t stream, int* launches);
+
+}  // namespace gemm_gb300

@@ -1,0 +1,501 @@
+// bf16 / fp16 GEMM on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// The tiling idea is the one "Learning to develop for GPU with GEMM as the example"
+// builds up (sections "Making the GPU implementation better", "How loading into local
+// memory is organised", "Improving the solution and balancing memory work"): blocks of
+// A and B are staged in on-chip memory and multiplied into a block of accumulators that
+// never leaves the chip until the block is done.  On this GPU every level is done by the
+// hardware unit made for it:
+//   * global -> shared: the Tensor Memory Accelerator (cp.async.bulk.tensor) copies a
+//     128 x 64 tile of A and a 64 x 256 tile of B per k-block, 128-byte swizzled (the
+//     swizzle is what the page's padding does by hand against bank conflicts, section
+//     "How to do even better");
+//   * the multiply: tcgen05.mma (M=128, N=256, K=16) issued by one thread, reading both
+//     operands from shared memory through matrix descriptors;
+//   * the accumulators: a 128 x 256 fp32 block in tensor memory (TMEM), two of them, so
+//     the epilogue of one output tile overlaps the main loop of the next;
+//   * the epilogue ("Three X: large convolutions in PyTorch for training", section
+//     "CUTLASS": the step after the MMA that moves accumulators out): tcgen05.ld into
+//     registers, then vectorised stores of fp32 C.
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
+// warps 2..5 = epilogue.  A 4-stage ring of shared-memory buffers links producer and MMA
+// through mbarriers.  The grid is persistent (one CTA per SM) and walks output tiles in
+// groups of 16 tile-rows so that concurrently running tiles share A rows and B columns
+// in L2 ("CUDA overview: performance surprises", section "Parallelism first": enough
+// independent work per SM, no idle units).
+//
+// Every wait on an mbarrier is bounded (a wall-clock limit read from %globaltimer).  On
+// expiry the thread records an error code in the caller-visible status word, the CTA
+// waits (again bounded) for its own TMA copies and MMAs in flight, frees its TMEM and
+// returns; the host reads the code through gemm_get_device_status.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace gemm_gb300 {
+namespace {
+
+constexpr int BM = 128;              // rows of an output tile (TMEM lanes)
+constexpr int BN = 256;              // columns of an output tile (fp32 TMEM columns)
+constexpr int BK = 64;               // k per stage: 64 x 2 bytes = one 128-byte swizzle row
+constexpr int UMMA_K = 16;           // k of one tcgen05.mma for 16-bit inputs
+constexpr int STAGES = 4;
+constexpr int GROUP_M = 16;          // tile rows per raster group
+constexpr int THREADS = 192;
+constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KiB
+constexpr int B_BOX_N = 64;                  // TMA box width along N (128 bytes)
+constexpr int B_BOX_BYTES = B_BOX_N * BK * 2;  // 8 KiB
+constexpr int B_STAGE_BYTES = BN * BK * 2;   // 32 KiB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int TMEM_COLS = 2 * BN;            // two accumulators
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait until the phase with the given parity has completed; false after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem] . B[smem]; one thread issues it.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread i receives row (lane base + i).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading- and
+// stride-dimension byte offsets (all >> 4), descriptor version 1 (bit 46), 128-byte
+// swizzle (value 2 in bits 61..63).  Base offset 0: every swizzle atom starts on a
+// 1024-byte boundary.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, A K-major, B N-major (B is the
+// row-major K x N operand), M = 128, N = 256.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16)
+{
+    return (1u << 4)                         // D format: f32
+           | ((bf16 ? 1u : 0u) << 7)         // A format: bf16 = 1, f16 = 0
+           | ((bf16 ? 1u : 0u) << 10)        // B format
+           | (0u << 15)                      // A major: K
+           | (1u << 16)                      // B major: MN
+           | ((uint32_t)(BN >> 3) << 17)     // N >> 3
+           | ((uint32_t)(BM >> 4) << 24);    // M >> 4
+}
+
+struct TileCoord {
+    int m_blk, n_blk;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(int t, int m_blocks, int n_blocks)
+{
+    const int per_group = GROUP_M * n_blocks;
+    const int g = t / per_group;
+    const int first_m = g * GROUP_M;
+    const int gm = min(m_blocks - first_m, GROUP_M);
+    const int r = t - g * per_group;
+    return {first_m + r % gm, r / gm};
+}
+
+struct TcParams {
+    int M, N, K;
+    float* C;
+    int64_t ldc;
+    int m_blocks, n_blocks, num_tiles, k_blocks;
+    uint32_t idesc;
+    int vec_store;
+    int* status;
+    uint64_t limit_ns;
+};
+
+__device__ __forceinline__ void record_error(int* status, int code, volatile int* abort_flag)
+{
+    atomicCAS(status, 0, code);
+    *abort_flag = 1;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    uint8_t* smem_a = smem;
+    uint8_t* smem_b = smem + STAGES * A_STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* full_bar = bars;                    // [STAGES] TMA bytes landed
+    uint64_t* empty_bar = bars + STAGES;          // [STAGES] MMAs reading the stage done
+    uint64_t* tfull_bar = bars + 2 * STAGES;      // [2] accumulator complete
+    uint64_t* tempty_bar = bars + 2 * STAGES + 2; // [2] accumulator drained by the epilogue
+    uint64_t* drain_bar = bars + 2 * STAGES + 4;  // MMA issuer's final completion check
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull_bar[a]), 1);
+            mbar_init(smem_u32(&tempty_bar[a]), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(smem_u32(drain_bar), 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, last_parity = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (*abort_flag || !mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.limit_ns)) {
+                        record_error(p.status, kDevTimeoutProducer, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full_bar[stage]);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    tma_load_2d(smem_u32(smem_a + stage * A_STAGE_BYTES), &tmA, fb, kb * BK, tc.m_blk * BM);
+                    uint8_t* b_dst = smem_b + stage * B_STAGE_BYTES;
+#pragma unroll
+                    for (int j = 0; j < BN / B_BOX_N; ++j)
+                        tma_load_2d(smem_u32(b_dst + j * B_BOX_BYTES), &tmB, fb, tc.n_blk * BN + j * B_BOX_N, kb * BK);
+                    issued_mask |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // every copy this CTA issued must have landed before its shared memory goes away
+            for (int s = 0; s < STAGES; ++s)
+                if ((issued_mask >> s) & 1)
+                    if (!mbar_wait(smem_u32(&full_bar[s]), (last_parity >> s) & 1, p.limit_ns))
+                        record_error(p.status, kDevTimeoutDrain, abort_flag);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            const uint32_t a_base = smem_u32(smem_a), b_base = smem_u32(smem_b);
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                if (*abort_flag || !mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, p.limit_ns)) {
+                    record_error(p.status, kDevTimeoutMma, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (*abort_flag || !mbar_wait(smem_u32(&full_bar[stage]), phase, p.limit_ns)) {
+                        record_error(p.status, kDevTimeoutMma, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_st = a_base + stage * A_STAGE_BYTES;
+                    const uint32_t b_st = b_base + stage * B_STAGE_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        // A: K-major rows of 128 bytes, 8-row atoms 1024 bytes apart; step k
+                        //    moves 32 bytes along the row inside the swizzle atom.
+                        const uint64_t a_desc = smem_desc_sw128(a_st + k * UMMA_K * 2, 16, 1024);
+                        // B: N-major, 8 k-rows of 128 bytes per atom; atoms 1024 bytes apart
+                        //    along K, 64-column boxes 8 KiB apart along N; step k = 16 rows.
+                        const uint64_t b_desc = smem_desc_sw128(b_st + k * UMMA_K * 128, B_BOX_BYTES, 1024);
+                        umma_f16(d_tmem, a_desc, b_desc, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(smem_u32(&empty_bar[stage]));  // stage free once these MMAs finish
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&tfull_bar[acc]));  // accumulator ready for the epilogue
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            // no MMA of this CTA may still be running when TMEM and shared memory are released
+            umma_commit(smem_u32(drain_bar));
+            if (!mbar_wait(smem_u32(drain_bar), 0, p.limit_ns)) record_error(p.status, kDevTimeoutDrain, abort_flag);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            bool ok = !*abort_flag && mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, p.limit_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) record_error(p.status, kDevTimeoutEpilogue, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
+            const int row = tc.m_blk * BM + q * 32 + lane;
+            const bool row_ok = row < p.M;
+            float* crow = p.C + (int64_t)row * p.ldc;
+            const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_row + c * 32, v);
+                tmem_ld_wait();
+                const int col0 = tc.n_blk * BN + c * 32;
+                if (row_ok) {
+                    if (p.vec_store && col0 + 31 < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            float4 f = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                   __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                            *reinterpret_cast<float4*>(crow + col0 + j) = f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < p.N) crow[col0 + j] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// Row-major [rows][cols] 16-bit matrix with row stride `ld` elements; box = box_cols x box_rows.
+bool encode_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uint64_t cols, uint64_t ld,
+               uint32_t box_cols, uint32_t box_rows)
+{
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_limit_ns, cudaStream_t stream,
+                   int* launches)
+{
+    // sizes must fit the kernel's 32-bit tile arithmetic and TMA's 32-bit coordinates
+    if (a.M > (1ll << 31) - BM || a.N > (1ll << 31) - BN || a.K > (1ll << 31) - BK) return GEMM_ERR_UNSUPPORTED;
+    CUtensorMap tmA, tmB;
+    const bool bf16 = a.is_bf16 != 0;
+    if (!encode_2d(&tmA, a.A, bf16, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda, BK, BM) ||
+        !encode_2d(&tmB, a.B, bf16, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.ldb, B_BOX_N, BK))
+        return GEMM_ERR_CUDA;
+    if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+        cudaSuccess)
+        return GEMM_ERR_CUDA;
+    TcParams p;
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.m_blocks = (int)((a.M + BM - 1) / BM);
+    p.n_blocks = (int)((a.N + BN - 1) / BN);
+    const int64_t tiles = (int64_t)p.m_blocks * p.n_blocks;
+    if (tiles > 0x7fffffffLL) return GEMM_ERR_UNSUPPORTED;
+    p.num_tiles = (int)tiles;
+    p.k_blocks = (int)((a.K + BK - 1) / BK);
+    p.idesc = make_idesc(bf16);
+    p.vec_store = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && (a.ldc % 4 == 0);
+    p.status = dev_status;
+    p.limit_ns = wait_limit_ns;
+    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+    tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, p);
+    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+    *launches += 1;
+    return GEMM_OK;
+}
+
+}  // namespace gemm_gb300

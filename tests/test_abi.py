@@ -1,0 +1,78 @@
+"""The C ABI library loads and exports every symbol include/gemm.h declares.
+
+Host-side checks only: argument validation that returns before any CUDA call, status
+strings, and option parsing.  No kernel is launched and no GPU is needed.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm.h")
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import programming_tiled_gemm_gb300 as p
+    return p
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = declared_functions()
+    for n in ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "conv4d_im2col",
+              "gemm_get_device_status", "gemm_set_option", "gemm_launch_count", "gemm_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(pkg):
+    lib = ctypes.CDLL(pkg.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), "missing export " + name
+    assert sorted(pkg.EXPORTS) == sorted(declared_functions())
+
+
+def test_exports_are_plain_c_symbols(pkg):
+    out = subprocess.run(["nm", "-D", "--defined-only", pkg.LIB_PATH], capture_output=True, text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in syms, name
+
+
+def test_status_strings(pkg):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert pkg.status_string(code) not in ("", "unknown status")
+    assert pkg.status_string(12345) == "unknown status"
+
+
+def test_null_handle_is_rejected_without_touching_cuda(pkg):
+    lib = pkg.library()
+    assert lib.gemm_run(None, 4, 4, 4, 1, 4, 1, 4, 1, 4, 0, None) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_run_host(None, 4, 4, 4, 1, 4, 1, 4, 1, 4, 0, None) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_set_option(None, 1, 0) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_get_device_status(None, None) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_destroy(None) == pkg.GEMM_OK
+    assert lib.gemm_create(None, 0) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_launch_count(None) == -1
+    ins = (ctypes.c_int64 * 4)(4, 4, 4, 4)
+    assert lib.conv4d_im2col(None, 1, 1, ins, ins, 1, None) == pkg.GEMM_ERR_INVALID_ARG
+
+
+def test_create_without_a_gpu_reports_an_error(pkg):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    rc = pkg.library().gemm_create(ctypes.byref(h), 0)
+    assert rc in (pkg.GEMM_ERR_CUDA, pkg.GEMM_ERR_INVALID_ARG)
+    assert not h.value

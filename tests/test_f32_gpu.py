@@ -1,0 +1,187 @@
+"""fp32 path on the GPU against the CPU oracle (through the C ABI).
+
+Tolerances (max |C - C_ref| over the compared entries):
+  * integer-valued inputs in [-4, 4]: exact (every partial sum is an integer below 2^24);
+  * uniform[-1, 1] inputs: 1e-5 * sqrt(K).
+Kernels: the 128x128 and 64x128 tiled FFMA kernels (with and without split-K) and the
+skinny streaming kernel, each forced on shapes with ragged tails, padded leading
+dimensions and guard bands around C.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 1234.5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import programming_tiled_gemm_gb300 as g
+    h = g.Gemm(0)
+    yield h
+    h.close()
+
+
+@pytest.fixture(autouse=True)
+def _reset_options(lib):
+    import programming_tiled_gemm_gb300 as g
+    yield
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, 0)
+    lib.set_option(g.GEMM_OPT_SPLIT_K, 0)
+
+
+def run_padded(lib, A, B, pad_a=0, pad_b=0, pad_c=0, guard=2):
+    """Run with leading dimensions padded and a sentinel band around C; check the band."""
+    dev = torch.device("cuda")
+    M, K = A.shape
+    N = B.shape[1]
+    Ad = torch.full((M, K + pad_a), float("nan"), device=dev)
+    Ad[:, :K] = A.to(dev)
+    Bd = torch.full((K, N + pad_b), float("nan"), device=dev)
+    Bd[:, :N] = B.to(dev)
+    Cbig = torch.full((M + 2 * guard, N + pad_c + 2 * guard), SENTINEL, device=dev)
+    Cv = Cbig[guard:guard + M, guard:guard + N]
+    lib.matmul(Ad[:, :K], Bd[:, :N], out=Cv)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    host = Cbig.cpu()
+    mask = torch.ones_like(host, dtype=torch.bool)
+    mask[guard:guard + M, guard:guard + N] = False
+    assert torch.all(host[mask] == SENTINEL), "kernel wrote outside C"
+    return host[guard:guard + M, guard:guard + N].double().numpy()
+
+
+def ref_of(A, B):
+    return oracle.gemm(A.numpy(), B.numpy())
+
+
+KERNELS = [(1, 0), (1, 3), (2, 0), (2, 2), (3, 0), (3, 5)]  # (kernel, split-K: 0 = auto)
+
+
+@pytest.mark.parametrize("kernel,split", KERNELS)
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (7, 13, 5), (31, 129, 67), (32, 1030, 300), (130, 257, 129)])
+def test_integer_inputs_are_exact(lib, kernel, split, M, N, K):
+    import programming_tiled_gemm_gb300 as g
+    if kernel == 3 and M > 32:
+        pytest.skip("skinny kernel takes M <= 32")
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, kernel)
+    lib.set_option(g.GEMM_OPT_SPLIT_K, split)
+    A, B = si.integer_copy(M, N, K, seed=M * 1000 + N + K)
+    got = run_padded(lib, A, B, pad_a=3, pad_b=5, pad_c=1)
+    assert np.array_equal(got, ref_of(A, B))
+
+
+@pytest.mark.parametrize("kernel,split", KERNELS)
+@pytest.mark.parametrize("M,N,K", [(17, 100, 1000), (29, 515, 777), (200, 136, 520)])
+def test_uniform_inputs_within_tolerance(lib, kernel, split, M, N, K):
+    import programming_tiled_gemm_gb300 as g
+    if kernel == 3 and M > 32:
+        pytest.skip("skinny kernel takes M <= 32")
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, kernel)
+    lib.set_option(g.GEMM_OPT_SPLIT_K, split)
+    A, B = si.gemm_operands(M, N, K, seed=5)
+    got = run_padded(lib, A, B, pad_b=4)
+    assert np.abs(got - ref_of(A, B)).max() <= 1e-5 * math.sqrt(K)
+
+
+def test_misaligned_operands_take_the_scalar_path(lib):
+    dev = torch.device("cuda")
+    M, N, K = 45, 61, 39
+    A, B = si.integer_copy(M, N, K, seed=3)
+    buf_a = torch.zeros(M * K + 1, device=dev)
+    buf_a[1:] = A.reshape(-1).to(dev)
+    buf_b = torch.zeros(K * N + 1, device=dev)
+    buf_b[1:] = B.reshape(-1).to(dev)
+    Ad = buf_a[1:].view(M, K)  # 4-byte offset: no float4 loads
+    Bd = buf_b[1:].view(K, N)
+    C = lib.matmul(Ad, Bd)
+    assert np.array_equal(C.cpu().double().numpy(), ref_of(A, B))
+
+
+def test_zero_K_writes_zeros_and_empty_shapes_are_noops(lib):
+    dev = torch.device("cuda")
+    C = torch.full((5, 7), 3.0, device=dev)
+    lib.matmul(torch.empty((5, 0), device=dev), torch.empty((0, 7), device=dev), out=C)
+    assert torch.all(C == 0)
+    C = torch.full((0, 7), 3.0, device=dev)
+    lib.matmul(torch.empty((0, 4), device=dev), torch.empty((4, 7), device=dev), out=C)
+    C = torch.full((3, 2), 3.0, device=dev)
+    lib.matmul(torch.ones((3, 4), device=dev)[:, :0], torch.ones((0, 2), device=dev), out=C)
+    assert torch.all(C == 0)
+
+
+def test_config_256_uniform_and_integer_copy(lib):
+    w = si.WORKLOADS["f32_256"]
+    A, B = si.workload_operands(w)
+    C = lib.matmul(A.cuda(), B.cuda())
+    assert np.abs(C.cpu().double().numpy() - ref_of(A, B)).max() <= 1e-5 * math.sqrt(w.K)
+    Ai, Bi = si.integer_copy(w.M, w.N, w.K, w.seed)
+    C = lib.matmul(Ai.cuda(), Bi.cuda())
+    assert np.array_equal(C.cpu().double().numpy(), ref_of(Ai, Bi))
+
+
+@pytest.mark.slow
+def test_config_4096_full_matrix(lib):
+    w = si.WORKLOADS["f32_4096"]
+    A, B = si.workload_operands(w)
+    C = lib.matmul(A.cuda(), B.cuda()).cpu().double().numpy()
+    assert np.abs(C - ref_of(A, B)).max() <= 1e-5 * math.sqrt(w.K)
+    Ai, Bi = si.integer_copy(w.M, w.N, w.K, w.seed)
+    C = lib.matmul(Ai.cuda(), Bi.cuda()).cpu().double().numpy()
+    assert np.array_equal(C, ref_of(Ai, Bi))
+
+
+@pytest.mark.slow
+def test_config_skinny_full_matrix(lib):
+    w = si.WORKLOADS["f32_skinny"]
+    A, B = si.workload_operands(w)
+    C = lib.matmul(A.cuda(), B.cuda()).cpu().double().numpy()
+    assert np.abs(C - ref_of(A, B)).max() <= 1e-5 * math.sqrt(w.K)
+    # |partial sums| <= 16 * 16384 < 2^24: integer inputs are exact at this K too
+    Ai, Bi = si.integer_copy(w.M, w.N, w.K, w.seed)
+    C = lib.matmul(Ai.cuda(), Bi.cuda()).cpu().double().numpy()
+    assert np.array_equal(C, ref_of(Ai, Bi))
+
+
+def test_results_are_deterministic(lib):
+    import programming_tiled_gemm_gb300 as g
+    A, B = si.gemm_operands(24, 3000, 5000, seed=9)
+    Ad, Bd = A.cuda(), B.cuda()
+    for kernel in (1, 2, 3):
+        lib.set_option(g.GEMM_OPT_F32_KERNEL, kernel)
+        lib.set_option(g.GEMM_OPT_SPLIT_K, 7)
+        c1 = lib.matmul(Ad, Bd).clone()
+        c2 = lib.matmul(Ad, Bd)
+        assert torch.equal(c1, c2)
+
+
+def test_argument_errors_are_reported(lib):
+    import programming_tiled_gemm_gb300 as g
+    dev = torch.device("cuda")
+    A = torch.ones((4, 4), device=dev)
+    C = torch.empty((4, 4), device=dev)
+    h = lib.handle
+    assert g.gemm_run(h, -1, 4, 4, A.data_ptr(), 4, A.data_ptr(), 4, C.data_ptr(), 4, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_run(h, 4, 4, 4, A.data_ptr(), 3, A.data_ptr(), 4, C.data_ptr(), 4, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_run(h, 4, 4, 4, A.data_ptr(), 4, A.data_ptr(), 4, C.data_ptr(), 3, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_run(h, 4, 4, 4, 0, 4, A.data_ptr(), 4, C.data_ptr(), 4, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_run(h, 4, 4, 4, A.data_ptr(), 4, A.data_ptr(), 4, C.data_ptr(), 4, 7) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_set_option(h, g.GEMM_OPT_F32_KERNEL, 9) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_set_option(h, g.GEMM_OPT_SPLIT_K, 5000) == g.GEMM_ERR_INVALID_ARG
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, 3)
+    assert g.gemm_run(h, 40, 4, 4, A.data_ptr(), 4, A.data_ptr(), 4, C.data_ptr(), 4, 0) == g.GEMM_ERR_UNSUPPORTED
+
+
+def test_host_buffer_entry_point(lib):
+    A, B = si.integer_copy(70, 90, 110, seed=4)
+    C = lib.matmul_host(A, B)
+    assert np.array_equal(C.double().numpy(), ref_of(A, B))
