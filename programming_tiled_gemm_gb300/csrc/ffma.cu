@@ -209,6 +209,195 @@ ffma_tiled_kernel(F32Args p, int64_t k_per_split, int m_tiles, int n_tiles, floa
     }
 }
 
+// 128 x 128 x 16 block tile, 256 threads as 2 x 4 warps of 64 x 32; inside a warp the
+// lanes form an 8 x 4 grid and each owns two 4 x 4 blocks per dimension (rows
+// ty*4 + {0,32}, columns tx*4 + {0,16}), so every fragment read is one shared-memory
+// wavefront and every float4 store row is 64 contiguous bytes per 4 lanes.
+// Two instantiations: EDGE = false for tiles wholly inside M x N with K a multiple of 16
+// and aligned operands (no predicates, running pointers), EDGE = true for everything
+// else (predicated, zero-filled loads).  The host launches the interior tiles and the
+// L-shaped edge region separately.
+constexpr int W_BM = 128, W_BN = 128, W_BK = 16;
+int g_warptile_min_blocks = 2;  // resident blocks per SM the interior kernel is compiled for
+
+struct TileMap {
+    int mode;        // 0: grouped raster over rows x cols tiles; 1: L-shaped edge region
+    int rows, cols;  // mode 0: tile grid; mode 1: full tile rows / cols (interior extent)
+    int m_tiles, n_tiles;
+};
+
+__device__ __forceinline__ void map_tile(const TileMap& t, int pid, int& mt, int& nt)
+{
+    if (t.mode == 0) {
+        const int width = kGroupM * t.cols;
+        const int group = pid / width;
+        const int first_m = group * kGroupM;
+        const int gsize = min(t.rows - first_m, kGroupM);
+        mt = first_m + (pid % width) % gsize;
+        nt = (pid % width) / gsize;
+    } else {
+        const int bottom = (t.m_tiles - t.rows) * t.n_tiles;  // partial tile rows, all columns
+        if (pid < bottom) {
+            mt = t.rows + pid / t.n_tiles;
+            nt = pid % t.n_tiles;
+        } else {
+            const int j = pid - bottom, w = t.n_tiles - t.cols;  // partial columns, full rows
+            mt = j / w;
+            nt = t.cols + j % w;
+        }
+    }
+}
+
+template <int MIN_BLOCKS, bool EDGE>
+__global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
+ffma_warptile_kernel(F32Args p, int64_t k_per_split, TileMap tmap, float* ws, int vec_in, int vec_out)
+{
+    constexpr int AS_LD = W_BM + 4;
+    __shared__ __align__(16) float As[2][W_BK][AS_LD];
+    __shared__ __align__(16) float Bs[2][W_BK][W_BN];
+
+    const int tid = threadIdx.x;
+    int mt, nt;
+    map_tile(tmap, blockIdx.x, mt, nt);
+    const int64_t m0 = (int64_t)mt * W_BM, n0 = (int64_t)nt * W_BN;
+    const int64_t kbeg = (int64_t)blockIdx.z * k_per_split;
+    const int64_t kend = min(p.K, kbeg + k_per_split);
+
+    float* out;
+    int64_t ldo;
+    if (gridDim.z > 1) {
+        out = ws + (int64_t)blockIdx.z * p.M * p.N;
+        ldo = p.N;
+    } else {
+        out = p.C;
+        ldo = p.ldc;
+    }
+
+    // global -> register staging: A float4s at (row a_row, k a_kq) and (a_row, a_kq + 8);
+    // B float4s at (k b_k, cols b_nq..+3) and (b_k + 8, b_nq..+3)
+    const int a_row = tid % W_BM, a_kq = (tid / W_BM) * 4;
+    const int b_k = tid / 32, b_nq = (tid % 32) * 4;
+    const bool a_ok = !EDGE || (m0 + a_row) < p.M;
+    const float* a_cur = p.A + (a_ok ? (m0 + a_row) : 0) * p.lda + kbeg + a_kq;
+    const float* b_cur = p.B + (kbeg + b_k) * p.ldb + n0 + b_nq;
+    const int64_t b_half = 8 * p.ldb;
+
+    float4 ra[2], rb[2];
+    int64_t k_next = kbeg;  // k of the tile the next load() fetches
+    auto load = [&]() {
+        if constexpr (!EDGE) {
+            ra[0] = __ldg(reinterpret_cast<const float4*>(a_cur));
+            ra[1] = __ldg(reinterpret_cast<const float4*>(a_cur + 8));
+            rb[0] = __ldg(reinterpret_cast<const float4*>(b_cur));
+            rb[1] = __ldg(reinterpret_cast<const float4*>(b_cur + b_half));
+        } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                const int64_t gk = k_next + a_kq + h * 8;
+                if (a_ok) {
+                    const float* src = a_cur + h * 8;
+                    if (vec_in && gk + 3 < kend) {
+                        v = __ldg(reinterpret_cast<const float4*>(src));
+                    } else {
+                        if (gk + 0 < kend) v.x = __ldg(src + 0);
+                        if (gk + 1 < kend) v.y = __ldg(src + 1);
+                        if (gk + 2 < kend) v.z = __ldg(src + 2);
+                        if (gk + 3 < kend) v.w = __ldg(src + 3);
+                    }
+                }
+                ra[h] = v;
+                v = make_float4(0.f, 0.f, 0.f, 0.f);
+                const int64_t bk = k_next + b_k + h * 8;
+                const int64_t gn = n0 + b_nq;
+                if (bk < kend) {
+                    const float* src = b_cur + h * b_half;
+                    if (vec_in && gn + 3 < p.N) {
+                        v = __ldg(reinterpret_cast<const float4*>(src));
+                    } else {
+                        if (gn + 0 < p.N) v.x = __ldg(src + 0);
+                        if (gn + 1 < p.N) v.y = __ldg(src + 1);
+                        if (gn + 2 < p.N) v.z = __ldg(src + 2);
+                        if (gn + 3 < p.N) v.w = __ldg(src + 3);
+                    }
+                }
+                rb[h] = v;
+            }
+            k_next += W_BK;
+        }
+        a_cur += W_BK;
+        b_cur += 2 * b_half;
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            // a warp holds 32 consecutive rows of one k: conflict-free transposed stores
+            As[buf][a_kq + h * 8 + 0][a_row] = ra[h].x;
+            As[buf][a_kq + h * 8 + 1][a_row] = ra[h].y;
+            As[buf][a_kq + h * 8 + 2][a_row] = ra[h].z;
+            As[buf][a_kq + h * 8 + 3][a_row] = ra[h].w;
+            *reinterpret_cast<float4*>(&Bs[buf][b_k + h * 8][b_nq]) = rb[h];
+        }
+    };
+
+    const int warp = tid / 32, lane = tid % 32;
+    const int wm = warp / 4, wn = warp % 4;  // 2 x 4 warps
+    const int ty = lane / 4, tx = lane % 4;  // 8 x 4 lanes
+    const int a_frag = wm * 64 + ty * 4;     // rows a_frag + {0..3}, a_frag + 32 + {0..3}
+    const int b_frag = wn * 32 + tx * 4;     // cols b_frag + {0..3}, b_frag + 16 + {0..3}
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    const int ktiles = (kend > kbeg) ? (int)((kend - kbeg + W_BK - 1) / W_BK) : 0;
+    if (ktiles > 0) {
+        load();
+        store(0);
+        __syncthreads();
+    }
+    for (int kt = 0; kt < ktiles; ++kt) {
+        const int buf = kt & 1;
+        if (kt + 1 < ktiles) load();  // in flight during the FFMAs below
+#pragma unroll
+        for (int k = 0; k < W_BK; ++k) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][a_frag]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][a_frag + 32]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][b_frag]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][b_frag + 16]);
+            const float af[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bf[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(af[i], bf[j], acc[i][j]);
+        }
+        if (kt + 1 < ktiles) store(buf ^ 1);
+        __syncthreads();
+    }
+
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t gm = m0 + a_frag + (i / 4) * 32 + (i % 4);
+        if (EDGE && gm >= p.M) continue;
+        float* row = out + gm * ldo;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t gn = n0 + b_frag + h * 16;
+            const float* v = &acc[i][h * 4];
+            if (vec_out && (!EDGE || gn + 3 < p.N)) {
+                *reinterpret_cast<float4*>(row + gn) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (gn + j < p.N) row[gn + j] = v[j];
+            }
+        }
+    }
+}
+
 // Fixed-order sum of split-K partials: C[m][n] = ws[0][m][n] + ws[1][m][n] + ...
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float* __restrict__ ws, int split, int64_t M, int64_t N,
@@ -254,11 +443,61 @@ cudaError_t launch_variant(const F32Args& a, int split, float* ws, cudaStream_t 
     return launch_splitk_reduce(ws, nsplit, a.M, a.N, a.C, a.ldc, 0, stream);
 }
 
+template <int MIN_BLOCKS>
+cudaError_t launch_warptile_occ(const F32Args& a, int64_t kps, int nsplit, float* ws, int vec_in, int vec_out,
+                                cudaStream_t stream, int* launches)
+{
+    const int m_tiles = (int)((a.M + W_BM - 1) / W_BM), n_tiles = (int)((a.N + W_BN - 1) / W_BN);
+    const int m_full = (int)(a.M / W_BM), n_full = (int)(a.N / W_BN);
+    const bool fast_ok = vec_in && (a.K % W_BK == 0);
+    const int interior = fast_ok ? m_full * n_full : 0;
+    const int64_t edge = (int64_t)m_tiles * n_tiles - interior;
+    if (interior > 0) {
+        TileMap t{0, m_full, n_full, m_tiles, n_tiles};
+        ffma_warptile_kernel<MIN_BLOCKS, false><<<dim3(interior, 1, nsplit), kThreads, 0, stream>>>(
+            a, kps, t, ws, vec_in, vec_out);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        *launches += 1;
+    }
+    if (edge > 0) {
+        TileMap t = fast_ok ? TileMap{1, m_full, n_full, m_tiles, n_tiles} : TileMap{0, m_tiles, n_tiles, m_tiles, n_tiles};
+        ffma_warptile_kernel<MIN_BLOCKS, true><<<dim3((unsigned)edge, 1, nsplit), kThreads, 0, stream>>>(
+            a, kps, t, ws, vec_in, vec_out);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        *launches += 1;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_warptile(const F32Args& a, int split, float* ws, cudaStream_t stream, int* launches)
+{
+    const int64_t m_tiles = (a.M + W_BM - 1) / W_BM, n_tiles = (a.N + W_BN - 1) / W_BN;
+    if (m_tiles * n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    int64_t kps = (a.K + split - 1) / split;
+    kps = (kps + W_BK - 1) / W_BK * W_BK;
+    const int nsplit = (int)((a.K + kps - 1) / kps);
+    const int vec_in = ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15) == 0 &&
+                       a.lda % 4 == 0 && a.ldb % 4 == 0;
+    int vec_out;
+    if (nsplit > 1)
+        vec_out = (a.N % 4 == 0);
+    else
+        vec_out = (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0;
+    cudaError_t e = (g_warptile_min_blocks == 1)
+                        ? launch_warptile_occ<1>(a, kps, nsplit, ws, vec_in, vec_out, stream, launches)
+                        : launch_warptile_occ<2>(a, kps, nsplit, ws, vec_in, vec_out, stream, launches);
+    if (e != cudaSuccess || nsplit == 1) return e;
+    *launches += 1;
+    return launch_splitk_reduce(ws, nsplit, a.M, a.N, a.C, a.ldc, 0, stream);
+}
+
 }  // namespace
 
 int ffma_auto_split(const F32Args& a, int variant, int num_sms)
 {
-    const int BM = (variant == 2) ? 64 : 128, BN = 128, BK = (variant == 2) ? 16 : 8;
+    const int BM = (variant == 2) ? 64 : 128, BN = 128, BK = 16;
     const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
     const int64_t capacity = (int64_t)num_sms * 2;  // two resident blocks per SM
     if (tiles >= capacity) return 1;
@@ -274,7 +513,7 @@ cudaError_t launch_ffma_tiled(const F32Args& a, int variant, int split, float* w
     (void)num_sms;
     if (split < 1) split = 1;
     if (variant == 2) return launch_variant<64, 128, 16, 4, 8>(a, split, ws, stream, launches);
-    return launch_variant<128, 128, 8, 8, 8>(a, split, ws, stream, launches);
+    return launch_warptile(a, split, ws, stream, launches);
 }
 
 cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t N, float* C,

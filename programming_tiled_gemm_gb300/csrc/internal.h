@@ -63,7 +63,8 @@ struct TcArgs {
     int is_bf16;  // 1 = bf16, 0 = fp16
 };
 // Returns GEMM_OK or a negative gemm_status_t.
-int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_limit_ns,
+// kc_blocks: 64-wide k-blocks per accumulation chunk (0 = default 16).
+int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_limit_ns, int kc_blocks,
                    cudaStream_t stream, int* launches);
 
 }  // namespace gemm_gb300

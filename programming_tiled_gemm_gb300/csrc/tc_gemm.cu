@@ -12,14 +12,22 @@
 //     "How to do even better");
 //   * the multiply: tcgen05.mma (M=128, N=256, K=16) issued by one thread, reading both
 //     operands from shared memory through matrix descriptors;
-//   * the accumulators: a 128 x 256 fp32 block in tensor memory (TMEM), two of them, so
-//     the epilogue of one output tile overlaps the main loop of the next;
+//   * the accumulators: a 128 x 256 fp32 block in tensor memory (TMEM).  The tensor
+//     core's own fp32 accumulation rounds toward zero, so its error grows faster than
+//     the length of the sum (measured on GB300: max error 4.5e-3 at K = 8192 for
+//     normal(0,1) bf16 inputs, against 2.6e-4 .. 6.2e-4 when the sum is cut into
+//     512- to 1024-long pieces).  The K loop is therefore cut into chunks of `kc`
+//     k-blocks: each chunk starts a fresh TMEM accumulator, alternating between two
+//     TMEM buffers, and the epilogue warps add every finished chunk into fp32
+//     registers with ordinary round-to-nearest adds, in chunk order;
 //   * the epilogue ("Three X: large convolutions in PyTorch for training", section
 //     "CUTLASS": the step after the MMA that moves accumulators out): tcgen05.ld into
-//     registers, then vectorised stores of fp32 C.
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
-// warps 2..5 = epilogue.  A 4-stage ring of shared-memory buffers links producer and MMA
-// through mbarriers.  The grid is persistent (one CTA per SM) and walks output tiles in
+//     registers, chunk sums in registers, then vectorised stores of fp32 C once the
+//     tile's last chunk is in.  While it works on one chunk, the MMA fills the other
+//     buffer, so the epilogue is hidden behind the main loop.
+// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
+// warps 2..9 = epilogue (two warps per 32-lane TMEM quarter, 128 columns each).  A
+// 4-stage ring of shared-memory buffers links producer and MMA through mbarriers.  The grid is persistent (one CTA per SM) and walks output tiles in
 // groups of 16 tile-rows so that concurrently running tiles share A rows and B columns
 // in L2 ("CUDA overview: performance surprises", section "Parallelism first": enough
 // independent work per SM, no idle units).
@@ -44,13 +52,15 @@ constexpr int BK = 64;               // k per stage: 64 x 2 bytes = one 128-byte
 constexpr int UMMA_K = 16;           // k of one tcgen05.mma for 16-bit inputs
 constexpr int STAGES = 4;
 constexpr int GROUP_M = 16;          // tile rows per raster group
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;        // two per TMEM lane quarter, each owning 128 columns
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_COLS = BN / 2;     // columns per epilogue thread (fp32 registers)
 constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KiB
 constexpr int B_BOX_N = 64;                  // TMA box width along N (128 bytes)
 constexpr int B_BOX_BYTES = B_BOX_N * BK * 2;  // 8 KiB
 constexpr int B_STAGE_BYTES = BN * BK * 2;   // 32 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int TMEM_COLS = 2 * BN;            // two accumulators
+constexpr int TMEM_COLS = 2 * BN;            // two chunk accumulators
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -222,6 +232,8 @@ struct TcParams {
     float* C;
     int64_t ldc;
     int m_blocks, n_blocks, num_tiles, k_blocks;
+    int kc;       // k-blocks per accumulation chunk
+    int nchunks;  // chunks per tile
     uint32_t idesc;
     int vec_store;
     int* status;
@@ -246,8 +258,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
     uint64_t* full_bar = bars;                    // [STAGES] TMA bytes landed
     uint64_t* empty_bar = bars + STAGES;          // [STAGES] MMAs reading the stage done
-    uint64_t* tfull_bar = bars + 2 * STAGES;      // [2] accumulator complete
-    uint64_t* tempty_bar = bars + 2 * STAGES + 2; // [2] accumulator drained by the epilogue
+    uint64_t* tfull_bar = bars + 2 * STAGES;      // [2] chunk accumulator complete
+    uint64_t* tempty_bar = bars + 2 * STAGES + 2; // [2] chunk accumulator read by the epilogue
     uint64_t* drain_bar = bars + 2 * STAGES + 4;  // MMA issuer's final completion check
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -262,7 +274,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
-            mbar_init(smem_u32(&tempty_bar[a]), 4);  // one arrival per epilogue warp
+            mbar_init(smem_u32(&tempty_bar[a]), EPI_WARPS);  // one arrival per epilogue warp
         }
         mbar_init(smem_u32(drain_bar), 1);
         *abort_flag = 0;
@@ -320,47 +332,52 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
+            int buf = 0;
+            uint32_t buf_phase = 0;
             bool ok = true;
             const uint32_t a_base = smem_u32(smem_a), b_base = smem_u32(smem_b);
             for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-                if (*abort_flag || !mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, p.limit_ns)) {
-                    record_error(p.status, kDevTimeoutMma, abort_flag);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (*abort_flag || !mbar_wait(smem_u32(&full_bar[stage]), phase, p.limit_ns)) {
+                for (int ch = 0; ch < p.nchunks && ok; ++ch) {
+                    if (*abort_flag || !mbar_wait(smem_u32(&tempty_bar[buf]), buf_phase ^ 1, p.limit_ns)) {
                         record_error(p.status, kDevTimeoutMma, abort_flag);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_st = a_base + stage * A_STAGE_BYTES;
-                    const uint32_t b_st = b_base + stage * B_STAGE_BYTES;
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                    const int kb0 = ch * p.kc;
+                    const int kb1 = min(kb0 + p.kc, p.k_blocks);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (*abort_flag || !mbar_wait(smem_u32(&full_bar[stage]), phase, p.limit_ns)) {
+                            record_error(p.status, kDevTimeoutMma, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_st = a_base + stage * A_STAGE_BYTES;
+                        const uint32_t b_st = b_base + stage * B_STAGE_BYTES;
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k) {
-                        // A: K-major rows of 128 bytes, 8-row atoms 1024 bytes apart; step k
-                        //    moves 32 bytes along the row inside the swizzle atom.
-                        const uint64_t a_desc = smem_desc_sw128(a_st + k * UMMA_K * 2, 16, 1024);
-                        // B: N-major, 8 k-rows of 128 bytes per atom; atoms 1024 bytes apart
-                        //    along K, 64-column boxes 8 KiB apart along N; step k = 16 rows.
-                        const uint64_t b_desc = smem_desc_sw128(b_st + k * UMMA_K * 128, B_BOX_BYTES, 1024);
-                        umma_f16(d_tmem, a_desc, b_desc, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            // A: K-major rows of 128 bytes, 8-row atoms 1024 bytes apart; step k
+                            //    moves 32 bytes along the row inside the swizzle atom.
+                            const uint64_t a_desc = smem_desc_sw128(a_st + k * UMMA_K * 2, 16, 1024);
+                            // B: N-major, 8 k-rows of 128 bytes per atom; atoms 1024 bytes apart
+                            //    along K, 64-column boxes 8 KiB apart along N; step k = 16 rows.
+                            const uint64_t b_desc = smem_desc_sw128(b_st + k * UMMA_K * 128, B_BOX_BYTES, 1024);
+                            umma_f16(d_tmem, a_desc, b_desc, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
+                        umma_commit(smem_u32(&empty_bar[stage]));  // stage free once these MMAs finish
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
                     }
-                    umma_commit(smem_u32(&empty_bar[stage]));  // stage free once these MMAs finish
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1;
+                    if (!ok) break;
+                    umma_commit(smem_u32(&tfull_bar[buf]));  // chunk sum ready for the epilogue
+                    if (++buf == 2) {
+                        buf = 0;
+                        buf_phase ^= 1;
                     }
-                }
-                if (!ok) break;
-                umma_commit(smem_u32(&tfull_bar[acc]));  // accumulator ready for the epilogue
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1;
                 }
             }
             // no MMA of this CTA may still be running when TMEM and shared memory are released
@@ -370,49 +387,60 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         __syncwarp();
     } else {
         // ---------------------------------------------------------------- epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        int acc = 0;
-        uint32_t acc_phase = 0;
+        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;  // which 128 of the tile's 256 columns
+        int buf = 0;
+        uint32_t buf_phase = 0;
+        float tot[EPI_COLS];
         for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-            bool ok = !*abort_flag && mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, p.limit_ns);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) record_error(p.status, kDevTimeoutEpilogue, abort_flag);
-                break;
-            }
-            tc_fence_after();
-            const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
-            const int row = tc.m_blk * BM + q * 32 + lane;
-            const bool row_ok = row < p.M;
-            float* crow = p.C + (int64_t)row * p.ldc;
-            const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(t_row + c * 32, v);
-                tmem_ld_wait();
-                const int col0 = tc.n_blk * BN + c * 32;
-                if (row_ok) {
-                    if (p.vec_store && col0 + 31 < p.N) {
+            bool ok = true;
+            for (int ch = 0; ch < p.nchunks; ++ch) {
+                ok = !*abort_flag && mbar_wait(smem_u32(&tfull_bar[buf]), buf_phase, p.limit_ns);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) record_error(p.status, kDevTimeoutEpilogue, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t t_addr =
+                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + half * EPI_COLS);
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            float4 f = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                                   __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-                            *reinterpret_cast<float4*>(crow + col0 + j) = f;
-                        }
+                for (int j = 0; j < EPI_COLS / 32; ++j) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(t_addr + j * 32, v);
+                    tmem_ld_wait();
+                    if (ch == 0) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) tot[j * 32 + i] = __uint_as_float(v[i]);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < p.N) crow[col0 + j] = __uint_as_float(v[j]);
+                        for (int i = 0; i < 32; ++i) tot[j * 32 + i] = __fadd_rn(tot[j * 32 + i], __uint_as_float(v[i]));
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf]));
+                if (++buf == 2) {
+                    buf = 0;
+                    buf_phase ^= 1;
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1;
+            if (!ok) break;
+            const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
+            const int row = tc.m_blk * BM + q * 32 + lane;
+            if (row < p.M) {
+                float* crow = p.C + (int64_t)row * p.ldc;
+                const int col0 = tc.n_blk * BN + half * EPI_COLS;
+                if (p.vec_store && col0 + EPI_COLS <= p.N) {
+#pragma unroll
+                    for (int j = 0; j < EPI_COLS; j += 4)
+                        *reinterpret_cast<float4*>(crow + col0 + j) =
+                            make_float4(tot[j], tot[j + 1], tot[j + 2], tot[j + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < EPI_COLS; ++j)
+                        if (col0 + j < p.N) crow[col0 + j] = tot[j];
+                }
             }
         }
     }
@@ -462,8 +490,8 @@ bool encode_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uin
 
 }  // namespace
 
-int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_limit_ns, cudaStream_t stream,
-                   int* launches)
+int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_limit_ns, int kc_blocks,
+                   cudaStream_t stream, int* launches)
 {
     // sizes must fit the kernel's 32-bit tile arithmetic and TMA's 32-bit coordinates
     if (a.M > (1ll << 31) - BM || a.N > (1ll << 31) - BN || a.K > (1ll << 31) - BK) return GEMM_ERR_UNSUPPORTED;
@@ -487,6 +515,8 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     if (tiles > 0x7fffffffLL) return GEMM_ERR_UNSUPPORTED;
     p.num_tiles = (int)tiles;
     p.k_blocks = (int)((a.K + BK - 1) / BK);
+    p.kc = kc_blocks > 0 ? kc_blocks : 16;
+    p.nchunks = (p.k_blocks + p.kc - 1) / p.kc;
     p.idesc = make_idesc(bf16);
     p.vec_store = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && (a.ldc % 4 == 0);
     p.status = dev_status;

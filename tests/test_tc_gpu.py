@@ -1,0 +1,163 @@
+"""bf16 / fp16 tensor-core path (tcgen05) on the GPU against the CPU oracle, via the C ABI.
+
+Tolerances (max |C - C_ref|):
+  * integer-valued inputs in [-4, 4] (exact in bf16 and fp16; every partial sum is an
+    integer below 2^24): exact;
+  * normal(0, 1) inputs rounded to bf16, compared with the oracle on the same rounded
+    values: 2e-5 * sqrt(K).
+At 8192^3 the oracle cannot do all 6.7e7 entries one by one in seconds, so the full-size
+test compares 128 full rows, 128 full columns and 65536 random entries exactly against
+the oracle, and checks the whole matrix with Freivalds' test: for random x,
+|C x - A (B x)| per row is bounded by sqrt(N) times the per-entry tolerance (the
+per-entry errors are independent across columns) plus the fp64 rounding of A (B x).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+
+pytestmark = pytest.mark.gpu
+SENTINEL = -777.25
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import programming_tiled_gemm_gb300 as g
+    h = g.Gemm(0)
+    yield h
+    h.close()
+
+
+@pytest.fixture(autouse=True)
+def _reset(lib):
+    import programming_tiled_gemm_gb300 as g
+    yield
+    lib.set_option(g.GEMM_OPT_TC_CHUNK, 0)
+
+
+def padded(t, ld, dev):
+    buf = torch.zeros((t.shape[0], ld), dtype=t.dtype, device=dev)
+    buf[:, : t.shape[1]] = t.to(dev)
+    return buf[:, : t.shape[1]]
+
+
+def run_guarded(lib, A, B, guard=3, pad_c=5):
+    dev = torch.device("cuda")
+    M, K = A.shape
+    N = B.shape[1]
+    Ad = padded(A, (K + 7) // 8 * 8 + 8, dev)
+    Bd = padded(B, (N + 7) // 8 * 8 + 16, dev)
+    Cbig = torch.full((M + 2 * guard, N + pad_c + 2 * guard), SENTINEL, device=dev)
+    Cv = Cbig[guard:guard + M, guard:guard + N]
+    lib.matmul(Ad, Bd, out=Cv)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    host = Cbig.cpu()
+    mask = torch.ones_like(host, dtype=torch.bool)
+    mask[guard:guard + M, guard:guard + N] = False
+    assert torch.all(host[mask] == SENTINEL), "kernel wrote outside C"
+    return host[guard:guard + M, guard:guard + N].double().numpy()
+
+
+SHAPES = [(1, 1, 1), (128, 256, 64), (128, 256, 16), (129, 257, 65), (200, 300, 100), (64, 1000, 8),
+          (256, 512, 1024), (1000, 24, 520), (1024, 2048, 512), (2048, 4096, 384)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_integer_inputs_exact(lib, dtype, M, N, K):
+    A, B = si.integer_copy(M, N, K, seed=M + 3 * N + 7 * K, dtype=dtype)
+    got = run_guarded(lib, A, B)
+    assert np.array_equal(got, oracle.gemm(A.float().numpy(), B.float().numpy()))
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 16, 4096])
+def test_accumulation_chunks_exact(lib, chunk):
+    import programming_tiled_gemm_gb300 as g
+    lib.set_option(g.GEMM_OPT_TC_CHUNK, chunk)
+    A, B = si.integer_copy(300, 520, 1100, seed=chunk)
+    got = run_guarded(lib, A, B)
+    assert np.array_equal(got, oracle.gemm(A.float().numpy(), B.float().numpy()))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (384, 256, 4096), (200, 300, 8192)])
+def test_normal_bf16_within_tolerance(lib, M, N, K):
+    A, B = si.gemm_operands(M, N, K, seed=21, dist="normal", dtype="bf16")
+    got = run_guarded(lib, A, B)
+    err = np.abs(got - oracle.gemm(A.float().numpy(), B.float().numpy())).max()
+    assert err <= 2e-5 * math.sqrt(K), err
+
+
+def test_results_are_deterministic(lib):
+    A, B = si.gemm_operands(1024, 2048, 2048, seed=5, dist="normal", dtype="bf16")
+    Ad, Bd = A.cuda(), B.cuda()
+    c1 = lib.matmul(Ad, Bd).clone()
+    c2 = lib.matmul(Ad, Bd)
+    assert torch.equal(c1, c2)
+
+
+def test_alignment_rules(lib):
+    import programming_tiled_gemm_gb300 as g
+    dev = torch.device("cuda")
+    buf = torch.zeros(64 * 72 + 8, dtype=torch.bfloat16, device=dev)
+    C = torch.empty((64, 64), device=dev)
+    B = torch.zeros((72, 64), dtype=torch.bfloat16, device=dev)
+    h = lib.handle
+    # A base 2 bytes off a 16-byte boundary
+    assert g.gemm_run(h, 64, 64, 72, buf.data_ptr() + 2, 72, B.data_ptr(), 64, C.data_ptr(), 64,
+                      g.GEMM_BF16) == g.GEMM_ERR_ALIGNMENT
+    # lda not a multiple of 8 elements
+    assert g.gemm_run(h, 64, 64, 70, buf.data_ptr(), 70, B.data_ptr(), 64, C.data_ptr(), 64,
+                      g.GEMM_BF16) == g.GEMM_ERR_ALIGNMENT
+    # the aligned call succeeds
+    assert g.gemm_run(h, 64, 64, 72, buf.data_ptr(), 72, B.data_ptr(), 64, C.data_ptr(), 64,
+                      g.GEMM_BF16) == g.GEMM_OK
+    torch.cuda.synchronize()
+
+
+def test_zero_K_and_empty(lib):
+    dev = torch.device("cuda")
+    C = torch.full((4, 8), 5.0, device=dev)
+    lib.matmul(torch.empty((4, 0), dtype=torch.bfloat16, device=dev),
+               torch.empty((0, 8), dtype=torch.bfloat16, device=dev), out=C)
+    assert torch.all(C == 0)
+
+
+def test_host_buffer_entry_point_bf16(lib):
+    A, B = si.integer_copy(130, 250, 190, seed=8, dtype="bf16")
+    C = lib.matmul_host(A, B)
+    assert np.array_equal(C.double().numpy(), oracle.gemm(A.float().numpy(), B.float().numpy()))
+
+
+@pytest.mark.slow
+def test_config_8192_sampled_and_freivalds(lib):
+    w = si.WORKLOADS["bf16_8192"]
+    A, B = si.workload_operands(w)
+    C = lib.matmul(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    tol = 2e-5 * math.sqrt(w.K)
+    Af, Bf = A.float().numpy(), B.float().numpy()
+    Cd = C.cpu().double().numpy()
+    rows, cols, ri, rj = si.sample_indices(w.M, w.N, w.seed)
+    rows, cols, ri, rj = rows.numpy(), cols.numpy(), ri.numpy(), rj.numpy()
+    err_rows = np.abs(Cd[rows] - oracle.gemm(Af[rows], Bf)).max()
+    err_cols = np.abs(Cd[:, cols] - oracle.gemm(Af, np.ascontiguousarray(Bf[:, cols]))).max()
+    err_rand = np.abs(Cd[ri, rj] - oracle.gemm_entries(Af, None, ri, rj,
+                                                       B_transposed_copy=np.ascontiguousarray(Bf.T))).max()
+    assert max(err_rows, err_cols, err_rand) <= tol, (err_rows, err_cols, err_rand)
+    # Freivalds: every row of C x against A (B x), x with entries +-1
+    g = np.random.default_rng(2)
+    A64, B64 = Af.astype(np.float64), Bf.astype(np.float64)
+    for _ in range(2):
+        x = g.choice([-1.0, 1.0], size=w.N)
+        lhs = Cd @ x
+        rhs = A64 @ (B64 @ x)
+        bound = tol * math.sqrt(w.N) * 6 + 1e-9 * np.abs(A64) @ np.abs(B64 @ x)
+        assert np.all(np.abs(lhs - rhs) <= bound)
