@@ -159,8 +159,8 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"tc_gemm": ["tc_gemm.cu"], "ffma_tiled": ["ffma.cu"], "skinny": ["skinny.cu", "ffma.cu"],
-                  "im2col4d": ["im2col.cu"]}
+KERNEL_SOURCES = {"tc_gemm": ["tc_gemm.cu", "internal.h"], "ffma_tiled": ["ffma.cu", "internal.h"],
+                  "skinny": ["skinny.cu", "ffma.cu", "internal.h"], "im2col4d": ["im2col.cu", "internal.h"]}
 
 
 def recorded_traffic(kernel: str, units: float):
