@@ -128,6 +128,37 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value);
  * count kept on the host; -1 for a NULL handle).  Zero-size calls launch nothing. */
 int64_t gemm_launch_count(gemm_handle_t h);
 
+/* fp32 C = A . B for M <= 32 (the skinny streaming kernel) WITHOUT ALLOCATING.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers that must
+ * not allocate device memory: code that runs inside another framework's memory
+ * manager (which already owns the device memory and forbids or cannot satisfy
+ * cudaMalloc), or a latency-critical path where cudaMalloc / cudaFree would
+ * synchronise the device.  Such a caller cannot create a gemm handle either (that
+ * allocates), so this call takes no handle and runs on the calling thread's current
+ * device, on `stream` (NULL = legacy default stream), asynchronously.
+ *
+ * The split-K partial sums live in a file-scope device array of 8,388,608 floats
+ * (32 MiB) inside the library; every GPU that loads the library's device code holds
+ * it until the process exits.  The call never calls cudaMalloc, cudaFree or any
+ * allocating library routine.
+ *   - The FIRST call on each device looks up that array's device address
+ *     (cudaGetSymbolAddress, which may load the library's device code); make that
+ *     first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents: two
+ *     calls that can run at the same time on the GPU (different streams, or
+ *     different host threads) race on it and both results are then undefined.
+ *     Serialise them on one stream.  Nothing needs clearing between calls: every
+ *     partial sum is written before it is read.
+ * Arguments as in gemm_run with dtype GEMM_F32; split_k = 0 picks the same split as
+ * gemm_run does by default (so results are bit-identical to gemm_run), 1..1024
+ * forces one.  Errors: GEMM_ERR_INVALID_ARG for bad arguments, GEMM_ERR_UNSUPPORTED
+ * for M > 32, for a device that is not sm_103, or when split_k * M * N exceeds the
+ * 8,388,608-float scratch array (the size limit); nothing is written then. */
+int gemm_run_f32_skinny_noalloc(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                                const float* B, int64_t ldb, float* C, int64_t ldc, int split_k,
+                                void* stream);
+
 /* Static string describing a status code. */
 const char* gemm_status_string(int status);
 

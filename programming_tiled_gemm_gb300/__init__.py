@@ -24,7 +24,8 @@ GEMM_OPT_F32_KERNEL, GEMM_OPT_SPLIT_K, GEMM_OPT_WAIT_LIMIT_US, GEMM_OPT_TC_CHUNK
 
 # Every symbol include/gemm.h declares (the ABI test checks the library exports them).
 EXPORTS = ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "conv4d_im2col",
-           "gemm_get_device_status", "gemm_set_option", "gemm_launch_count", "gemm_status_string"]
+           "gemm_get_device_status", "gemm_set_option", "gemm_launch_count", "gemm_status_string",
+           "gemm_run_f32_skinny_noalloc"]
 
 
 class GemmError(RuntimeError):
@@ -46,6 +47,7 @@ def _load():
     lib.gemm_get_device_status.argtypes = [p, p]
     lib.gemm_set_option.argtypes = [p, i32, i64]
     lib.gemm_launch_count.argtypes = [p]
+    lib.gemm_run_f32_skinny_noalloc.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, i32, p]
     lib.gemm_status_string.argtypes = [i32]
     lib.gemm_status_string.restype = ctypes.c_char_p
     for name in EXPORTS:
