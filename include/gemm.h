@@ -118,9 +118,11 @@ typedef enum {
     GEMM_OPT_F32_KERNEL = 1, /* 0 auto, 1 tiled 128x128 FFMA, 2 tiled 64x128 FFMA, 3 skinny streaming (M<=32) */
     GEMM_OPT_SPLIT_K = 2,    /* 0 auto, else the split-K factor for fp32 kernels (1..1024) */
     GEMM_OPT_WAIT_LIMIT_US = 3, /* 0 default (2 s), else the bounded-wait limit of device waits in microseconds */
-    GEMM_OPT_TC_CHUNK = 4       /* 0 default (16), else the tensor-core accumulation chunk in 64-wide k-blocks
+    GEMM_OPT_TC_CHUNK = 4,      /* 0 default (16), else the tensor-core accumulation chunk in 64-wide k-blocks
                                    (1..4096): the tensor core's fp32 accumulator is restarted every chunk and
                                    chunk sums are added in fp32 round-to-nearest */
+    GEMM_OPT_TC_PAIR = 5        /* tensor-core tiles: 0 choose (default: pairs when M > 128), 1 one CTA per
+                                   128x256 tile, 2 a pair of CTAs (cluster of two) per 256x256 tile */
 } gemm_option_t;
 int gemm_set_option(gemm_handle_t h, int option, int64_t value);
 

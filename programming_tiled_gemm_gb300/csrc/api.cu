@@ -26,6 +26,7 @@ struct gemm_ctx {
     int opt_f32_kernel = 0;
     int opt_split_k = 0;
     int opt_tc_chunk = 0;  // tensor-core accumulation chunk in 64-wide k-blocks (0 = default)
+    int opt_tc_pair = 0;   // tensor-core tile: 0 choose, 1 single CTA, 2 CTA pair
     uint64_t wait_limit_ns = 2000000000ull;
     int64_t launches = 0;  // kernels launched through this handle
 };
@@ -176,6 +177,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
         if (value < 0 || value > 4096) return GEMM_ERR_INVALID_ARG;
         h->opt_tc_chunk = (int)value;
         return GEMM_OK;
+    case GEMM_OPT_TC_PAIR:
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+        h->opt_tc_pair = (int)value;
+        return GEMM_OK;
     case GEMM_OPT_WAIT_LIMIT_US:
         if (value < 0 || value > 60000000) return GEMM_ERR_INVALID_ARG;
         h->wait_limit_ns = value == 0 ? 2000000000ull : (uint64_t)value * 1000ull;
@@ -207,7 +212,7 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, in
     }
     TcArgs t{M, N, K, A, lda, B, ldb, C, ldc, dtype == GEMM_BF16 ? 1 : 0};
     int n = 0;
-    int rc2 = launch_tc_gemm(t, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_tc_chunk, s, &n);
+    int rc2 = launch_tc_gemm(t, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_tc_chunk, h->opt_tc_pair, s, &n);
     h->launches += n;
     return rc2;
 }

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(256) im2col4d_kernel(const float* __restrict__
                 v.y = __ldg(src + 1);
                 v.z = __ldg(src + 2);
                 v.w = __ldg(src + 3);
-                *reinterpret_cast<float4*>(dst_row + n0) = v;
+                __stcs(reinterpret_cast<float4*>(dst_row + n0), v);  // streamed: read later, L2 would not hold it
             } else {
                 for (int j = 0; j < 4 && n0 + j < g.ncols; ++j) {
                     const int n = n0 + j;
@@ -82,7 +82,6 @@ __global__ void __launch_bounds__(256) im2col4d_kernel(const float* __restrict__
 cudaError_t launch_im2col4d(const float* x, int64_t cin, const int64_t in[4], const int64_t k[4],
                             float* col, int num_sms, cudaStream_t stream)
 {
-    (void)num_sms;
     const int64_t p0 = in[0] - k[0] + 1, p1 = in[1] - k[1] + 1, p2 = in[2] - k[2] + 1, p3 = in[3] - k[3] + 1;
     const int64_t ncols = p0 * p1 * p2 * p3;
     if (ncols >= (1ll << 31) - 4) return cudaErrorInvalidValue;
@@ -94,8 +93,16 @@ cudaError_t launch_im2col4d(const float* x, int64_t cin, const int64_t in[4], co
     g.p1 = (int)p1, g.p2 = (int)p2, g.p3 = (int)p3;
     g.chan_stride = in[0] * in[1] * in[2] * in[3];
     const int quads = (g.ncols + 3) / 4;
-    const unsigned gx = (unsigned)((quads + 255) / 256);
-    const unsigned gy = (unsigned)(g.nrows < 65535 ? g.nrows : 65535);
+    // a few thousand long-lived blocks: each thread walks several float4s of a row and
+    // several rows (grid-stride in both directions)
+    int64_t gx64 = (quads + 1023) / 1024;
+    if (gx64 < 1) gx64 = 1;
+    const unsigned gx = (unsigned)gx64;
+    int64_t gy64 = (int64_t)(num_sms > 0 ? num_sms : 152) * 16 / gx64;
+    if (gy64 < 1) gy64 = 1;
+    if (gy64 > g.nrows) gy64 = g.nrows;
+    if (gy64 > 65535) gy64 = 65535;
+    const unsigned gy = (unsigned)gy64;
     const bool quad = (p3 % 4 == 0) && (reinterpret_cast<uintptr_t>(col) & 15) == 0;
     if (quad)
         im2col4d_kernel<true><<<dim3(gx, gy), 256, 0, stream>>>(x, g, col);

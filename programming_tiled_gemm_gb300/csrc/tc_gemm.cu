@@ -201,8 +201,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A K-major, B N-major (B is the
-// row-major K x N operand), M = 128, N = 256.
-__host__ __device__ constexpr uint32_t make_idesc(bool bf16)
+// row-major K x N operand), N = 256; M = 128 for one CTA, 256 for a CTA pair.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int m = BM)
 {
     return (1u << 4)                         // D format: f32
            | ((bf16 ? 1u : 0u) << 7)         // A format: bf16 = 1, f16 = 0
@@ -210,7 +210,7 @@ __host__ __device__ constexpr uint32_t make_idesc(bool bf16)
            | (0u << 15)                      // A major: K
            | (1u << 16)                      // B major: MN
            | ((uint32_t)(BN >> 3) << 17)     // N >> 3
-           | ((uint32_t)(BM >> 4) << 24);    // M >> 4
+           | ((uint32_t)(m >> 4) << 24);     // M >> 4
 }
 
 struct TileCoord {
@@ -453,6 +453,345 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
 }
 
+
+// ============================================================================ CTA pair
+// The same pipeline on a pair of CTAs (a cluster of two, one per SM of a TPC) with
+// tcgen05's cta_group::2 MMAs: one instruction computes a 256 x 256 x 16 block, rows
+// 0..127 into the even CTA's TMEM and rows 128..255 into the odd CTA's.  Each CTA stages
+// only its own half of A (128 rows) and its own half of B (128 columns) in shared
+// memory; the pair's tensor cores read both halves.  Per SM that is 32 KiB of operands
+// per 64-deep k-block instead of 48 KiB, which is what limited the one-CTA kernel (its
+// shared-memory data path was saturated by operand reads plus TMA fills).
+// The even CTA's warp 1 issues every MMA; its commits arrive on barriers in both CTAs
+// (multicast).  Both CTAs' TMA loads complete on the even CTA's "full" barrier.  The odd
+// CTA's epilogue warps arrive remotely on the even CTA's "accumulator drained" barrier.
+constexpr int P_STAGES = 6;
+constexpr int P_A_STAGE_BYTES = BM * BK * 2;                     // 16 KiB: this CTA's 128 rows of A
+constexpr int P_B_STAGE_BYTES = (BN / 2) * BK * 2;               // 16 KiB: this CTA's 128 columns of B
+constexpr int P_STAGE_BYTES = P_A_STAGE_BYTES + P_B_STAGE_BYTES; // per CTA
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 1024;
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait (acquire at cluster scope); gives up early once `abort_flag` is set.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                  volatile int* abort_flag)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((abort_flag && *abort_flag) || global_timer() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the barrier at this shared-memory offset in both CTAs of the pair once every
+// tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar)
+{
+    const uint16_t both = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(bar), "h"(both)
+        : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on a barrier that
+// may live in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Spin (bounded by wall clock) so that copies and MMAs still in flight after an abort
+// can land before shared memory is released.
+__device__ __forceinline__ void grace_period(uint64_t ns)
+{
+    const uint64_t t0 = global_timer();
+    while (global_timer() - t0 < ns) {
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    uint8_t* smem_a = smem;
+    uint8_t* smem_b = smem + P_STAGES * P_A_STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    uint64_t* full_bar = bars;                       // [P_STAGES] (used in the even CTA)
+    uint64_t* empty_bar = bars + P_STAGES;           // [P_STAGES] (both CTAs, multicast)
+    uint64_t* tfull_bar = bars + 2 * P_STAGES;       // [2] (both CTAs, multicast)
+    uint64_t* tempty_bar = bars + 2 * P_STAGES + 2;  // [2] (used in the even CTA)
+    uint64_t* drain_bar = bars + 2 * P_STAGES + 4;   // (both CTAs, multicast)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull_bar[a]), 1);
+            mbar_init(smem_u32(&tempty_bar[a]), 2 * EPI_WARPS);  // epilogue warps of both CTAs
+        }
+        mbar_init(smem_u32(drain_bar), 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
+        tc_fence_before();
+    }
+    __syncthreads();
+    cluster_sync_all();  // the peer's barriers and TMEM exist before anything targets them
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    bool aborted = false;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = pair; t < p.num_tiles && ok; t += npairs) {
+                const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_cluster(smem_u32(&empty_bar[stage]), phase ^ 1, p.limit_ns, abort_flag)) {
+                        record_error(p.status, kDevTimeoutProducer, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb_local = smem_u32(&full_bar[stage]);
+                    const uint32_t fb_even = mapa_shared(fb_local, 0);
+                    if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
+                    tma_load_2d_pair(smem_u32(smem_a + stage * P_A_STAGE_BYTES), &tmA, fb_even, kb * BK,
+                                     tc.m_blk * (2 * BM) + (int)rank * BM);
+                    uint8_t* b_dst = smem_b + stage * P_B_STAGE_BYTES;
+#pragma unroll
+                    for (int j = 0; j < (BN / 2) / B_BOX_N; ++j)
+                        tma_load_2d_pair(smem_u32(b_dst + j * B_BOX_BYTES), &tmB, fb_even,
+                                         tc.n_blk * BN + (int)rank * (BN / 2) + j * B_BOX_N, kb * BK);
+                    if (++stage == P_STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) aborted = true;
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer (even CTA)
+        if (lane == 0 && rank == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t buf_phase = 0;
+            bool ok = true;
+            const uint32_t a_base = smem_u32(smem_a), b_base = smem_u32(smem_b);
+            const uint32_t idesc = p.idesc;
+            for (int t = pair; t < p.num_tiles && ok; t += npairs) {
+                for (int ch = 0; ch < p.nchunks && ok; ++ch) {
+                    if (!mbar_wait_cluster(smem_u32(&tempty_bar[buf]), buf_phase ^ 1, p.limit_ns, abort_flag)) {
+                        record_error(p.status, kDevTimeoutMma, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                    const int kb0 = ch * p.kc;
+                    const int kb1 = min(kb0 + p.kc, p.k_blocks);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait_cluster(smem_u32(&full_bar[stage]), phase, p.limit_ns, abort_flag)) {
+                            record_error(p.status, kDevTimeoutMma, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_st = a_base + stage * P_A_STAGE_BYTES;
+                        const uint32_t b_st = b_base + stage * P_B_STAGE_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            const uint64_t a_desc = smem_desc_sw128(a_st + k * UMMA_K * 2, 16, 1024);
+                            const uint64_t b_desc = smem_desc_sw128(b_st + k * UMMA_K * 128, B_BOX_BYTES, 1024);
+                            umma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
+                        umma_commit_pair(smem_u32(&empty_bar[stage]));
+                        if (++stage == P_STAGES) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit_pair(smem_u32(&tfull_bar[buf]));
+                    if (++buf == 2) {
+                        buf = 0;
+                        buf_phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) aborted = true;
+            umma_commit_pair(smem_u32(drain_bar));  // reaches both CTAs once every MMA is done
+        }
+        if (lane == 0) {
+            if (!mbar_wait_cluster(smem_u32(drain_bar), 0, p.limit_ns, nullptr)) {
+                record_error(p.status, kDevTimeoutDrain, abort_flag);
+                aborted = true;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- epilogue (both CTAs)
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        int buf = 0;
+        uint32_t buf_phase = 0;
+        float tot[EPI_COLS];
+        for (int t = pair; t < p.num_tiles; t += npairs) {
+            bool ok = true;
+            for (int ch = 0; ch < p.nchunks; ++ch) {
+                ok = mbar_wait_cluster(smem_u32(&tfull_bar[buf]), buf_phase, p.limit_ns, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) record_error(p.status, kDevTimeoutEpilogue, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t t_addr =
+                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + half * EPI_COLS);
+#pragma unroll
+                for (int j = 0; j < EPI_COLS / 32; ++j) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(t_addr + j * 32, v);
+                    tmem_ld_wait();
+                    if (ch == 0) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) tot[j * 32 + i] = __uint_as_float(v[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) tot[j * 32 + i] = __fadd_rn(tot[j * 32 + i], __uint_as_float(v[i]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[buf]), 0));
+                if (++buf == 2) {
+                    buf = 0;
+                    buf_phase ^= 1;
+                }
+            }
+            if (!ok) {
+                aborted = true;
+                break;
+            }
+            const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
+            const int row = tc.m_blk * (2 * BM) + (int)rank * BM + q * 32 + lane;
+            if (row < p.M) {
+                float* crow = p.C + (int64_t)row * p.ldc;
+                const int col0 = tc.n_blk * BN + half * EPI_COLS;
+                if (p.vec_store && col0 + EPI_COLS <= p.N) {
+#pragma unroll
+                    for (int j = 0; j < EPI_COLS; j += 4)
+                        *reinterpret_cast<float4*>(crow + col0 + j) =
+                            make_float4(tot[j], tot[j + 1], tot[j + 2], tot[j + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < EPI_COLS; ++j)
+                        if (col0 + j < p.N) crow[col0 + j] = tot[j];
+                }
+            }
+        }
+    }
+
+    // after an abort, give copies and MMAs already issued time to land before the pair's
+    // shared memory and TMEM are released
+    if (__syncthreads_or(aborted ? 1 : 0)) grace_period(2000000ull);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no MMA, remote arrival or TMA of the pair still targets this CTA
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -491,7 +830,7 @@ bool encode_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uin
 }  // namespace
 
 int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_limit_ns, int kc_blocks,
-                   cudaStream_t stream, int* launches)
+                   int pair_mode, cudaStream_t stream, int* launches)
 {
     // sizes must fit the kernel's 32-bit tile arithmetic and TMA's 32-bit coordinates
     if (a.M > (1ll << 31) - BM || a.N > (1ll << 31) - BN || a.K > (1ll << 31) - BK) return GEMM_ERR_UNSUPPORTED;
@@ -521,6 +860,33 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.vec_store = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && (a.ldc % 4 == 0);
     p.status = dev_status;
     p.limit_ns = wait_limit_ns;
+    // CTA pairs: 256 x 256 tiles on clusters of two; single CTAs: 128 x 256 tiles
+    const bool use_pair = (pair_mode == 2) || (pair_mode == 0 && a.M > BM && num_sms >= 2);
+    if (use_pair) {
+        p.m_blocks = (int)((a.M + 2 * BM - 1) / (2 * BM));
+        const int64_t ptiles = (int64_t)p.m_blocks * p.n_blocks;
+        p.num_tiles = (int)ptiles;
+        p.idesc = make_idesc(bf16, 2 * BM);
+        const int pairs = (int)(ptiles < num_sms / 2 ? ptiles : num_sms / 2);
+        if (cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
+            cudaSuccess)
+            return GEMM_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * pairs, 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = P_SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, tmA, tmB, p) != cudaSuccess) return GEMM_ERR_CUDA;
+        *launches += 1;
+        return GEMM_OK;
+    }
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
     tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, p);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
