@@ -115,7 +115,9 @@ int gemm_get_device_status(gemm_handle_t h, void* stream);
 /* Tuning and test options (see GEMM_OPT_*).  Values outside the documented range are
  * rejected with GEMM_ERR_INVALID_ARG.  Defaults are restored by passing 0. */
 typedef enum {
-    GEMM_OPT_F32_KERNEL = 1, /* 0 auto, 1 tiled 128x128 FFMA, 2 tiled 64x128 FFMA, 3 skinny streaming (M<=32) */
+    GEMM_OPT_F32_KERNEL = 1, /* 0 auto, 1 tiled 128x128 FFMA, 2 tiled 64x128 FFMA, 3 skinny streaming from
+                                registers (M<=32), 4 skinny streaming through a TMA ring (M<=32; B 16-byte
+                                aligned with ldb % 4 == 0, else GEMM_ERR_ALIGNMENT) */
     GEMM_OPT_SPLIT_K = 2,    /* 0 auto, else the split-K factor for fp32 kernels (1..1024) */
     GEMM_OPT_WAIT_LIMIT_US = 3, /* 0 default (2 s), else the bounded-wait limit of device waits in microseconds */
     GEMM_OPT_TC_CHUNK = 4,      /* 0 default (16), else the tensor-core accumulation chunk in 64-wide k-blocks
@@ -152,9 +154,11 @@ int64_t gemm_launch_count(gemm_handle_t h);
  *     different host threads) race on it and both results are then undefined.
  *     Serialise them on one stream.  Nothing needs clearing between calls: every
  *     partial sum is written before it is read.
- * Arguments as in gemm_run with dtype GEMM_F32; split_k = 0 picks the same split as
- * gemm_run does by default (so results are bit-identical to gemm_run), 1..1024
- * forces one.  Errors: GEMM_ERR_INVALID_ARG for bad arguments, GEMM_ERR_UNSUPPORTED
+ * It runs the register-streaming skinny kernel, the one gemm_run runs for M <= 32 with
+ * GEMM_OPT_F32_KERNEL = 3.  Arguments as in gemm_run with dtype GEMM_F32; split_k = 0
+ * picks the split gemm_run picks for that kernel (results are then bit-identical to
+ * gemm_run with that option; gemm_run's default TMA-fed kernel agrees within fp32
+ * rounding), 1..1024 forces one.  Errors: GEMM_ERR_INVALID_ARG for bad arguments, GEMM_ERR_UNSUPPORTED
  * for M > 32, for a device that is not sm_103, or when split_k * M * N exceeds the
  * 8,388,608-float scratch array (the size limit); nothing is written then. */
 int gemm_run_f32_skinny_noalloc(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,

@@ -94,11 +94,14 @@ int check_common(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A
 int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)
 {
     int kernel = h->opt_f32_kernel;
-    if (kernel == 0) kernel = (a.M <= 32) ? 3 : (a.M <= 64 ? 2 : 1);
-    if (kernel == 3 && a.M > 32) return GEMM_ERR_UNSUPPORTED;
+    if (kernel == 0) kernel = (a.M <= 32) ? (skinny_tma_supported(a) ? 4 : 3) : (a.M <= 64 ? 2 : 1);
+    if ((kernel == 3 || kernel == 4) && a.M > 32) return GEMM_ERR_UNSUPPORTED;
+    if (kernel == 4 && !skinny_tma_supported(a)) return GEMM_ERR_ALIGNMENT;
     int split = h->opt_split_k;
     if (split == 0)
-        split = (kernel == 3) ? skinny_auto_split(a, h->num_sms) : ffma_auto_split(a, kernel, h->num_sms);
+        split = (kernel == 4)   ? skinny_tma_auto_split(a, h->num_sms)
+                : (kernel == 3) ? skinny_auto_split(a, h->num_sms)
+                                : ffma_auto_split(a, kernel, h->num_sms);
     if ((int64_t)split > a.K) split = (int)(a.K > 0 ? a.K : 1);
     if (split > 1) {
         const size_t need = (size_t)split * (size_t)a.M * (size_t)a.N * sizeof(float);
@@ -107,7 +110,9 @@ int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)
     }
     cudaError_t e;
     int n = 0;
-    if (kernel == 3)
+    if (kernel == 4)
+        e = launch_skinny_tma(a, split, h->workspace, h->num_sms, h->d_status, h->wait_limit_ns, stream, &n);
+    else if (kernel == 3)
         e = launch_skinny(a, split, h->workspace, h->num_sms, stream, &n);
     else
         e = launch_ffma_tiled(a, kernel, split, h->workspace, h->num_sms, stream, &n);
@@ -166,7 +171,7 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     if (!h) return GEMM_ERR_INVALID_ARG;
     switch (option) {
     case GEMM_OPT_F32_KERNEL:
-        if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
+        if (value < 0 || value > 4) return GEMM_ERR_INVALID_ARG;
         h->opt_f32_kernel = (int)value;
         return GEMM_OK;
     case GEMM_OPT_SPLIT_K:

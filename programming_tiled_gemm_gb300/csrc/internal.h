@@ -37,6 +37,12 @@ cudaError_t launch_ffma_tiled(const F32Args& a, int variant, int split, float* w
 cudaError_t launch_skinny(const F32Args& a, int split, float* workspace, int num_sms,
                           cudaStream_t stream, int* launches);
 
+// fp32 skinny GEMM (M <= 32) with B streamed through a TMA ring in shared memory.
+bool skinny_tma_supported(const F32Args& a);
+int skinny_tma_auto_split(const F32Args& a, int num_sms);
+cudaError_t launch_skinny_tma(const F32Args& a, int split, float* workspace, int num_sms, int* dev_status,
+                              uint64_t limit_ns, cudaStream_t stream, int* launches);
+
 // Fixed-order split-K reduction: C[m][n] = sum_{s=0..split-1} ws[s][m][n].
 cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t N, float* C,
                                  int64_t ldc, int num_sms, cudaStream_t stream);

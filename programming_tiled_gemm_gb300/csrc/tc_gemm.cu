@@ -217,12 +217,12 @@ struct TileCoord {
     int m_blk, n_blk;
 };
 
-__device__ __forceinline__ TileCoord tile_coord(int t, int m_blocks, int n_blocks)
+__device__ __forceinline__ TileCoord tile_coord(int t, int m_blocks, int n_blocks, int group_m = GROUP_M)
 {
-    const int per_group = GROUP_M * n_blocks;
+    const int per_group = group_m * n_blocks;
     const int g = t / per_group;
-    const int first_m = g * GROUP_M;
-    const int gm = min(m_blocks - first_m, GROUP_M);
+    const int first_m = g * group_m;
+    const int gm = min(m_blocks - first_m, group_m);
     const int r = t - g * per_group;
     return {first_m + r % gm, r / gm};
 }
@@ -234,6 +234,7 @@ struct TcParams {
     int m_blocks, n_blocks, num_tiles, k_blocks;
     int kc;       // k-blocks per accumulation chunk
     int nchunks;  // chunks per tile
+    int group_m;  // tile rows per raster group
     uint32_t idesc;
     int vec_store;
     int* status;
@@ -465,11 +466,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // The even CTA's warp 1 issues every MMA; its commits arrive on barriers in both CTAs
 // (multicast).  Both CTAs' TMA loads complete on the even CTA's "full" barrier.  The odd
 // CTA's epilogue warps arrive remotely on the even CTA's "accumulator drained" barrier.
-constexpr int P_STAGES = 6;
+constexpr int P_STAGES_DEFAULT = 6;
 constexpr int P_A_STAGE_BYTES = BM * BK * 2;                     // 16 KiB: this CTA's 128 rows of A
 constexpr int P_B_STAGE_BYTES = (BN / 2) * BK * 2;               // 16 KiB: this CTA's 128 columns of B
 constexpr int P_STAGE_BYTES = P_A_STAGE_BYTES + P_B_STAGE_BYTES; // per CTA
-constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 1024;
+constexpr int p_smem_bytes(int stages) { return stages * P_STAGE_BYTES + 1024 + 1024; }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
@@ -576,6 +577,7 @@ __device__ __forceinline__ void grace_period(uint64_t ns)
     }
 }
 
+template <int P_STAGES>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p)
 {
@@ -631,7 +633,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t phase = 0;
             bool ok = true;
             for (int t = pair; t < p.num_tiles && ok; t += npairs) {
-                const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
+                const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks, p.group_m);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait_cluster(smem_u32(&empty_bar[stage]), phase ^ 1, p.limit_ns, abort_flag)) {
                         record_error(p.status, kDevTimeoutProducer, abort_flag);
@@ -761,7 +763,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 aborted = true;
                 break;
             }
-            const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
+            const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks, p.group_m);
             const int row = tc.m_blk * (2 * BM) + (int)rank * BM + q * 32 + lane;
             if (row < p.M) {
                 float* crow = p.C + (int64_t)row * p.ldc;
@@ -855,6 +857,7 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.num_tiles = (int)tiles;
     p.k_blocks = (int)((a.K + BK - 1) / BK);
     p.kc = kc_blocks > 0 ? kc_blocks : 16;
+    p.group_m = GROUP_M;
     p.nchunks = (p.k_blocks + p.kc - 1) / p.kc;
     p.idesc = make_idesc(bf16);
     p.vec_store = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && (a.ldc % 4 == 0);
@@ -868,13 +871,18 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
         p.num_tiles = (int)ptiles;
         p.idesc = make_idesc(bf16, 2 * BM);
         const int pairs = (int)(ptiles < num_sms / 2 ? ptiles : num_sms / 2);
-        if (cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
+        // 6 stages of 32 KiB; 7 measured no faster.  Raster groups of 8 pair-tile rows
+        // (2048 rows of C) measured best among 2, 4, 8 and 16, within run-to-run noise.
+        constexpr int stages = P_STAGES_DEFAULT;
+        p.group_m = 8;
+        auto kern = tc_gemm_pair_kernel<stages>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem_bytes(stages)) !=
             cudaSuccess)
             return GEMM_ERR_CUDA;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * pairs, 1, 1);
         cfg.blockDim = dim3(THREADS, 1, 1);
-        cfg.dynamicSmemBytes = P_SMEM_BYTES;
+        cfg.dynamicSmemBytes = p_smem_bytes(stages);
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -883,7 +891,7 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, tmA, tmB, p) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) return GEMM_ERR_CUDA;
         *launches += 1;
         return GEMM_OK;
     }

@@ -3,9 +3,10 @@
 Tolerances (max |C - C_ref| over the compared entries):
   * integer-valued inputs in [-4, 4]: exact (every partial sum is an integer below 2^24);
   * uniform[-1, 1] inputs: 1e-5 * sqrt(K).
-Kernels: the 128x128 and 64x128 tiled FFMA kernels (with and without split-K) and the
-skinny streaming kernel, each forced on shapes with ragged tails, padded leading
-dimensions and guard bands around C.
+Kernels: the 128x128 and 64x128 tiled FFMA kernels (with and without split-K) and the two
+skinny kernels (B streamed through registers, or through a TMA ring in shared memory),
+each forced on shapes with ragged tails, padded leading dimensions and guard bands
+around C.
 """
 import math
 
@@ -64,19 +65,20 @@ def ref_of(A, B):
     return oracle.gemm(A.numpy(), B.numpy())
 
 
-KERNELS = [(1, 0), (1, 3), (2, 0), (2, 2), (3, 0), (3, 5)]  # (kernel, split-K: 0 = auto)
+KERNELS = [(1, 0), (1, 3), (2, 0), (2, 2), (3, 0), (3, 5), (4, 0), (4, 5)]  # (kernel, split-K: 0 = auto)
 
 
 @pytest.mark.parametrize("kernel,split", KERNELS)
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (7, 13, 5), (31, 129, 67), (32, 1030, 300), (130, 257, 129)])
 def test_integer_inputs_are_exact(lib, kernel, split, M, N, K):
     import programming_tiled_gemm_gb300 as g
-    if kernel == 3 and M > 32:
-        pytest.skip("skinny kernel takes M <= 32")
+    if kernel in (3, 4) and M > 32:
+        pytest.skip("skinny kernels take M <= 32")
     lib.set_option(g.GEMM_OPT_F32_KERNEL, kernel)
     lib.set_option(g.GEMM_OPT_SPLIT_K, split)
     A, B = si.integer_copy(M, N, K, seed=M * 1000 + N + K)
-    got = run_padded(lib, A, B, pad_a=3, pad_b=5, pad_c=1)
+    # the TMA-fed kernel needs 16-byte B rows: pad ldb to a multiple of 4 floats
+    got = run_padded(lib, A, B, pad_a=3, pad_b=(4 - N % 4) % 4 + 4 if kernel == 4 else 5, pad_c=1)
     assert np.array_equal(got, ref_of(A, B))
 
 
@@ -84,12 +86,12 @@ def test_integer_inputs_are_exact(lib, kernel, split, M, N, K):
 @pytest.mark.parametrize("M,N,K", [(17, 100, 1000), (29, 515, 777), (200, 136, 520)])
 def test_uniform_inputs_within_tolerance(lib, kernel, split, M, N, K):
     import programming_tiled_gemm_gb300 as g
-    if kernel == 3 and M > 32:
-        pytest.skip("skinny kernel takes M <= 32")
+    if kernel in (3, 4) and M > 32:
+        pytest.skip("skinny kernels take M <= 32")
     lib.set_option(g.GEMM_OPT_F32_KERNEL, kernel)
     lib.set_option(g.GEMM_OPT_SPLIT_K, split)
     A, B = si.gemm_operands(M, N, K, seed=5)
-    got = run_padded(lib, A, B, pad_b=4)
+    got = run_padded(lib, A, B, pad_b=(4 - N % 4) % 4 + 4)
     assert np.abs(got - ref_of(A, B)).max() <= 1e-5 * math.sqrt(K)
 
 
@@ -156,7 +158,7 @@ def test_results_are_deterministic(lib):
     import programming_tiled_gemm_gb300 as g
     A, B = si.gemm_operands(24, 3000, 5000, seed=9)
     Ad, Bd = A.cuda(), B.cuda()
-    for kernel in (1, 2, 3):
+    for kernel in (1, 2, 3, 4):
         lib.set_option(g.GEMM_OPT_F32_KERNEL, kernel)
         lib.set_option(g.GEMM_OPT_SPLIT_K, 7)
         c1 = lib.matmul(Ad, Bd).clone()
@@ -179,6 +181,9 @@ def test_argument_errors_are_reported(lib):
     assert g.gemm_set_option(h, g.GEMM_OPT_SPLIT_K, 5000) == g.GEMM_ERR_INVALID_ARG
     lib.set_option(g.GEMM_OPT_F32_KERNEL, 3)
     assert g.gemm_run(h, 40, 4, 4, A.data_ptr(), 4, A.data_ptr(), 4, C.data_ptr(), 4, 0) == g.GEMM_ERR_UNSUPPORTED
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, 4)
+    # the TMA-fed kernel needs 16-byte aligned B rows
+    assert g.gemm_run(h, 4, 3, 4, A.data_ptr(), 4, A.data_ptr(), 3, C.data_ptr(), 4, 0) == g.GEMM_ERR_ALIGNMENT
 
 
 def test_host_buffer_entry_point(lib):

@@ -7,8 +7,9 @@ sums in a fixed 32 MiB array inside the library instead of an allocated workspac
 
 These tests call it through the C ABI (ctypes, no binding helper) twice in a row and
 compare each result with the existing entry point, gemm_run, on the same inputs, within
-the fp32 tolerance the other tests use (1e-5 * sqrt(K)); with the default split both run
-the same kernel with the same split, so the results are expected to be identical.
+the fp32 tolerance the other tests use (1e-5 * sqrt(K)).  With gemm_run told to use the
+same kernel (the register-streaming skinny kernel) and the default split, both run the
+same code with the same split, so those results are also expected to be identical.
 The file sorts last so that a run that stops at the first failure has run every other
 test first; it also passes on its own in a fresh process.
 """
@@ -58,7 +59,9 @@ def test_matches_gemm_run_on_two_calls_in_a_row(g, M, N, K, split_k):
     ref_lib = g.Gemm(0)
     if split_k:
         ref_lib.set_option(g.GEMM_OPT_SPLIT_K, split_k)
-    ref = ref_lib.matmul(Ad, Bd)
+    ref_default = ref_lib.matmul(Ad, Bd)  # gemm_run's default kernel choice
+    ref_lib.set_option(g.GEMM_OPT_F32_KERNEL, 3)
+    ref = ref_lib.matmul(Ad, Bd)  # the kernel this entry point runs
     torch.cuda.synchronize()
     tol = 1e-5 * math.sqrt(K)
     outs = []
@@ -68,6 +71,7 @@ def test_matches_gemm_run_on_two_calls_in_a_row(g, M, N, K, split_k):
         torch.cuda.synchronize()
         assert torch.isfinite(C).all()
         assert (C - ref).abs().max().item() <= tol
+        assert (C - ref_default).abs().max().item() <= tol
         outs.append(C)
     assert torch.equal(outs[0], outs[1])
     assert torch.equal(outs[0], ref)  # same kernel, same split: identical sums
