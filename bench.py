@@ -366,6 +366,12 @@ def measure_extras(lib, dev, stream, peaks, fp32_peak, reps=20):
                      "hbm_frac": round(bytes_gemm / ms / 1e6 / peaks["hbm_gbs"], 4),
                      "im2col_ms": round(ms_col, 4),
                      "im2col_hbm_frac": round(4 * w.K * w.N / ms_col / 1e6 / peaks["hbm_gbs"], 4)}
+    del col
+    w6 = wt.to(dev)
+    ms_imp = time_fn(lambda: lib.conv4d_implicit(xd, w6, out=y))
+    res["conv4d_implicit"] = {"ms": round(ms_imp, 4), "tflops": round(w.flops / ms_imp / 1e9, 2),
+                              "fp32_frac": round(w.flops / ms_imp / 1e9 / fp32_peak, 4), "bound": "alu",
+                              "vs_im2col_plus_gemm": round((ms_col + ms) / ms_imp, 2)}
     return res
 
 

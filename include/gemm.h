@@ -106,6 +106,21 @@ int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
 int conv4d_im2col(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4],
                   const int64_t k_dims[4], float* col, void* stream);
 
+/* The same valid 4-D cross-correlation computed directly, as an implicit GEMM: the
+ * column matrix of conv4d_im2col is never stored ("Three X: large convolutions in
+ * PyTorch for training", sections "CUTLASS" and "What else had to change when using
+ * CUTLASS": the operand tile is gathered from the input on the fly).
+ *   x : fp32 [C_in][in[0]][in[1]][in[2]][in[3]], contiguous, device memory.
+ *   w : fp32 [C_out][C_in][k[0]][k[1]][k[2]][k[3]], contiguous, device memory.
+ *   y : fp32 output, y[o][p] at y + o*ldy + p, p the row-major output position over
+ *       (P0, P1, P2, P3), Pd = in[d] - k[d] + 1; ldy >= P0*P1*P2*P3.  Overwritten.
+ * fp32 FMAs, accumulation order over taps (c, r0, r1, r2, r3) in slices added in fixed
+ * order: results are deterministic and agree with gemm_run(W, im2col(x)) within fp32
+ * rounding.  Asynchronous on `stream`; uses the handle's split-K workspace.
+ * GEMM_ERR_INVALID_ARG for bad extents or pointers; GEMM_ERR_UNSUPPORTED if k[3] > 40. */
+int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4], const float* w,
+                   int64_t C_out, const int64_t k_dims[4], float* y, int64_t ldy, void* stream);
+
 /* Synchronise `stream`, then read and clear the handle's device status word.
  * Returns GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a kernel launched through this
  * handle gave up on a bounded wait since the last call (its output is then invalid),

@@ -23,7 +23,7 @@ GEMM_ERR_DEVICE_TIMEOUT = -5
 GEMM_OPT_F32_KERNEL, GEMM_OPT_SPLIT_K, GEMM_OPT_WAIT_LIMIT_US, GEMM_OPT_TC_CHUNK, GEMM_OPT_TC_PAIR = 1, 2, 3, 4, 5
 
 # Every symbol include/gemm.h declares (the ABI test checks the library exports them).
-EXPORTS = ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "conv4d_im2col",
+EXPORTS = ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "conv4d_im2col", "conv4d_forward",
            "gemm_get_device_status", "gemm_set_option", "gemm_launch_count", "gemm_status_string",
            "gemm_run_f32_skinny_noalloc"]
 
@@ -44,6 +44,7 @@ def _load():
     lib.gemm_run.argtypes = [p, i64, i64, i64, p, i64, p, i64, p, i64, i32, p]
     lib.gemm_run_host.argtypes = [p, i64, i64, i64, p, i64, p, i64, p, i64, i32, p]
     lib.conv4d_im2col.argtypes = [p, p, i64, ctypes.POINTER(i64), ctypes.POINTER(i64), p, p]
+    lib.conv4d_forward.argtypes = [p, p, i64, ctypes.POINTER(i64), p, i64, ctypes.POINTER(i64), p, i64, p]
     lib.gemm_get_device_status.argtypes = [p, p]
     lib.gemm_set_option.argtypes = [p, i32, i64]
     lib.gemm_launch_count.argtypes = [p]
@@ -91,6 +92,12 @@ def conv4d_im2col(h, x, C_in, in_dims, k_dims, col, stream=0) -> int:
     ins = (ctypes.c_int64 * 4)(*[int(v) for v in in_dims])
     ks = (ctypes.c_int64 * 4)(*[int(v) for v in k_dims])
     return _lib.conv4d_im2col(h, x, C_in, ins, ks, col, stream)
+
+
+def conv4d_forward(h, x, C_in, in_dims, w, C_out, k_dims, y, ldy, stream=0) -> int:
+    ins = (ctypes.c_int64 * 4)(*[int(v) for v in in_dims])
+    ks = (ctypes.c_int64 * 4)(*[int(v) for v in k_dims])
+    return _lib.conv4d_forward(h, x, C_in, ins, w, C_out, ks, y, ldy, stream)
 
 
 def gemm_get_device_status(h, stream=0) -> int:
@@ -210,6 +217,27 @@ class Gemm:
             raise GemmError(rc, "conv4d_im2col")
         return col
 
+    def conv4d_implicit(self, x, w, out=None, stream=None):
+        """Valid 4-D cross-correlation as an implicit GEMM: y[C_out, P0, P1, P2, P3]."""
+        import torch
+        if x.dim() != 5 or w.dim() != 6 or x.dtype != torch.float32 or w.dtype != torch.float32:
+            raise ValueError("x must be fp32 [C_in, I0..I3] and w fp32 [C_out, C_in, R0..R3]")
+        if not (x.is_contiguous() and w.is_contiguous()):
+            raise ValueError("x and w must be contiguous")
+        cin, cout = x.shape[0], w.shape[0]
+        ks = list(w.shape[2:])
+        outs = [i - k + 1 for i, k in zip(x.shape[1:], ks)]
+        npos = outs[0] * outs[1] * outs[2] * outs[3]
+        if out is None:
+            out = torch.empty((cout, npos), dtype=torch.float32, device=x.device)
+        ldy = _row_major_2d(out, "out")
+        s = torch.cuda.current_stream(x.device).cuda_stream if stream is None else int(stream)
+        rc = conv4d_forward(self.handle, x.data_ptr(), cin, list(x.shape[1:]), w.data_ptr(), cout, ks,
+                            out.data_ptr(), ldy, s)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "conv4d_forward")
+        return out.view(cout, *outs) if out.is_contiguous() else out
+
     def conv4d(self, x, w, col=None, out=None, stream=None):
         """Valid 4-D cross-correlation as im2col + GEMM: y[C_out, P0, P1, P2, P3]."""
         ks = list(w.shape[2:])
@@ -229,6 +257,6 @@ class Gemm:
 
 
 __all__ = ["Gemm", "GemmError", "gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host",
-           "conv4d_im2col", "gemm_get_device_status", "gemm_set_option", "gemm_launch_count",
+           "conv4d_im2col", "conv4d_forward", "gemm_get_device_status", "gemm_set_option", "gemm_launch_count",
            "gemm_status_string",
            "status_string", "library", "LIB_PATH", "EXPORTS"]

@@ -273,6 +273,44 @@ int64_t gemm_launch_count(gemm_handle_t h)
     return h ? h->launches : -1;
 }
 
+int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4], const float* w,
+                   int64_t C_out, const int64_t k_dims[4], float* y, int64_t ldy, void* stream)
+{
+    if (!h || !x || !w || !y || !in_dims || !k_dims || C_in <= 0 || C_out <= 0) return GEMM_ERR_INVALID_ARG;
+    int64_t npos = 1, taps = C_in;
+    for (int d = 0; d < 4; ++d) {
+        if (in_dims[d] <= 0 || k_dims[d] <= 0 || k_dims[d] > in_dims[d] || in_dims[d] > (1 << 20))
+            return GEMM_ERR_INVALID_ARG;
+        npos *= in_dims[d] - k_dims[d] + 1;
+        taps *= k_dims[d];
+    }
+    if (ldy < npos || C_in > (1 << 20) || C_out > (1 << 20)) return GEMM_ERR_INVALID_ARG;
+    if (k_dims[3] > 40 || npos >= (1ll << 40) || C_in * k_dims[0] * k_dims[1] * k_dims[2] >= (1ll << 31))
+        return GEMM_ERR_UNSUPPORTED;
+    DeviceGuard g(h->device);
+    if (!g.ok()) return GEMM_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int ngroups = (int)(C_in * k_dims[0] * k_dims[1] * k_dims[2]);
+    int split = h->opt_split_k > 0 ? h->opt_split_k : conv_implicit_auto_split(npos, ngroups, h->num_sms);
+    if (split > ngroups) split = ngroups;
+    const int64_t cblock = C_out < 32 ? C_out : 32;
+    if (split > 1) {
+        const size_t need = (size_t)split * (size_t)cblock * (size_t)npos * sizeof(float);
+        int rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, need);
+        if (rc != GEMM_OK) return rc;
+    }
+    // output channels in blocks of 32 (rows of W and y)
+    for (int64_t o0 = 0; o0 < C_out; o0 += 32) {
+        const int64_t nc = (C_out - o0) < 32 ? (C_out - o0) : 32;
+        int n = 0;
+        cudaError_t e = launch_conv4d_implicit(x, C_in, in_dims, w + o0 * taps, nc, k_dims, y + o0 * ldy, ldy, split,
+                                               h->workspace, h->num_sms, s, &n);
+        h->launches += n;
+        if (e != cudaSuccess) return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
 int gemm_get_device_status(gemm_handle_t h, void* stream)
 {
     if (!h) return GEMM_ERR_INVALID_ARG;

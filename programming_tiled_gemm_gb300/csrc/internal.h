@@ -57,6 +57,13 @@ int skinny_auto_split(const F32Args& a, int num_sms);
 cudaError_t launch_im2col4d(const float* x, int64_t cin, const int64_t in[4], const int64_t k[4],
                             float* col, int num_sms, cudaStream_t stream);
 
+// Valid 4-D cross-correlation as an implicit GEMM (no column matrix), C_out <= 32 per
+// launch.  y[o][p] at y + o*ldy + p; split > 1 uses `workspace` ([split][cout][npos]).
+int conv_implicit_auto_split(int64_t npos, int ngroups, int num_sms);
+cudaError_t launch_conv4d_implicit(const float* x, int64_t cin, const int64_t in[4], const float* w,
+                                   int64_t cout, const int64_t k[4], float* y, int64_t ldy, int split,
+                                   float* workspace, int num_sms, cudaStream_t stream, int* launches);
+
 // bf16 / fp16 tensor-core GEMM (tcgen05 + TMA + TMEM), persistent.
 struct TcArgs {
     int64_t M, N, K;

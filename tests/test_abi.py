@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_header_declares_the_documented_entry_points():
     names = declared_functions()
-    for n in ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "conv4d_im2col",
+    for n in ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "conv4d_im2col", "conv4d_forward",
               "gemm_get_device_status", "gemm_set_option", "gemm_launch_count", "gemm_status_string"]:
         assert n in names
 
@@ -66,6 +66,7 @@ def test_null_handle_is_rejected_without_touching_cuda(pkg):
     assert lib.gemm_launch_count(None) == -1
     ins = (ctypes.c_int64 * 4)(4, 4, 4, 4)
     assert lib.conv4d_im2col(None, 1, 1, ins, ins, 1, None) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.conv4d_forward(None, 1, 1, ins, 1, 1, ins, 1, 1, None) == pkg.GEMM_ERR_INVALID_ARG
 
 
 def test_create_without_a_gpu_reports_an_error(pkg):
