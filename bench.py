@@ -159,8 +159,10 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"tc_gemm": ["tc_gemm.cu", "internal.h"], "ffma_tiled": ["ffma.cu", "internal.h"],
-                  "skinny": ["skinny.cu", "ffma.cu", "internal.h"], "im2col4d": ["im2col.cu", "internal.h"]}
+# the translation units whose device code a capture measured (a change there makes the
+# recorded DRAM traffic stale)
+KERNEL_SOURCES = {"tc_gemm": ["tc_gemm.cu"], "ffma_tiled": ["ffma.cu"], "skinny": ["skinny_tma.cu", "ffma.cu"],
+                  "im2col4d": ["im2col.cu"], "conv_implicit": ["conv_implicit.cu", "ffma.cu"]}
 
 
 def recorded_traffic(kernel: str, units: float):
@@ -199,7 +201,7 @@ def run_ours(args, rank, world, local_rank):
     shas = {}
     for n in names:
         w = si.WORKLOADS[n]
-        A, B = si.workload_operands(w)
+        A, B = si.workload_operands(w)  # for the convolution: (x, weights)
         shas[n] = si.sha256(A, B)[:16]
         Ad, Bd = A.to(dev), B.to(dev)
         Cd = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
@@ -208,7 +210,10 @@ def run_ours(args, rank, world, local_rank):
 
     def run_op(op):
         w, Ad, Bd, Cd = op
-        lib.matmul(Ad, Bd, out=Cd)
+        if w.kind == "conv4d":
+            lib.conv4d_implicit(Ad, Bd, out=Cd)  # implicit GEMM: y = W . col(x), no column matrix
+        else:
+            lib.matmul(Ad, Bd, out=Cd)
 
     for _ in range(args.warmup):
         for op in ops:
@@ -269,6 +274,10 @@ def run_ours(args, rank, world, local_rank):
         tflops = w.flops / (ms * 1e-3) / 1e12
         if w.dtype == "bf16":
             peak, bound, kname = peaks["bf16_tflops"], "tensor", "tc_gemm"
+        elif w.kind == "conv4d":
+            peak, bound, kname = fp32_peak, "alu", "conv_implicit"
+        elif w.M <= 32:
+            peak, bound, kname = fp32_peak, "alu", "skinny"
         else:
             peak, bound, kname = fp32_peak, "alu", "ffma_tiled"
         entry = {"ms": round(ms, 4), "tflops": round(tflops, 2), "peak_tflops": round(peak, 1),
@@ -381,12 +390,16 @@ def measure_e2e(lib, ops, args, dev, world, pg, reps=None):
     host = []
     h2d = d2h = 0
     for w, Ad, Bd, Cd in ops:
+        if w.kind != "gemm":
+            continue
         A = Ad.cpu().pin_memory()
         B = Bd.cpu().pin_memory()
         C = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
         host.append((w, A, B, C))
         h2d += A.numel() * A.element_size() + B.numel() * B.element_size()
         d2h += C.numel() * 4
+    if not host:
+        return None
     n = reps or max(3, min(args.steps, 20))
     for w, A, B, C in host:
         lib.matmul_host(A, B, out=C)
@@ -420,7 +433,9 @@ def oracle_sample(ops_cpu, rows_per_op):
 
 def cpu_baseline(ops, seconds):
     import numpy as np
-    ops_cpu = [(w, Ad.float().cpu().numpy(), Bd.float().cpu().numpy()) for w, Ad, Bd, _ in ops]
+    ops_cpu = [(w, Ad.float().cpu().numpy(), Bd.float().cpu().numpy()) for w, Ad, Bd, _ in ops if w.kind == "gemm"]
+    if not ops_cpu:
+        return None
     # calibrate on a small block, then size the sample to about `seconds`
     f0, t0 = oracle_sample(ops_cpu, [8] * len(ops_cpu))
     rate = f0 / max(t0, 1e-6)

@@ -123,13 +123,15 @@ __global__ void __launch_bounds__(CI_THREADS, 1) conv4d_implicit_kernel(ConvPara
         // stored to wsm[buf] (so the L2 latency overlaps the previous chunk's FMAs)
         float wreg[W_PER_THREAD];
         int64_t gb_reg = 0;
+        // element e of a chunk = (tap e / 32, output channel e % 32): a warp stores one tap
+        // row of 32 channels, conflict-free
         auto load_w = [&](int qc) {
 #pragma unroll
             for (int i = 0; i < W_PER_THREAD; ++i) {
                 const int e = tid + i * CI_THREADS;
                 float v = 0.f;
                 if (e < ntap_chunk * CI_MR) {
-                    const int tap = e % ntap_chunk, m = e / ntap_chunk;
+                    const int tap = e / CI_MR, m = e % CI_MR;
                     const int q = qc + tap / g.r3;
                     if (m < g.cout && q < q_end) v = __ldg(p.w + (int64_t)m * g.ntaps + (int64_t)q * g.r3 + tap % g.r3);
                 }
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(CI_THREADS, 1) conv4d_implicit_kernel(ConvPara
 #pragma unroll
             for (int i = 0; i < W_PER_THREAD; ++i) {
                 const int e = tid + i * CI_THREADS;
-                if (e < ntap_chunk * CI_MR) wsm[buf][e % ntap_chunk][e / ntap_chunk] = wreg[i];
+                if (e < ntap_chunk * CI_MR) wsm[buf][e / CI_MR][e % CI_MR] = wreg[i];
             }
             if (tid < gpc) gbase[buf][tid] = gb_reg;
         };
