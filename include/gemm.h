@@ -138,8 +138,14 @@ typedef enum {
     GEMM_OPT_TC_CHUNK = 4,      /* 0 default (16), else the tensor-core accumulation chunk in 64-wide k-blocks
                                    (1..4096): the tensor core's fp32 accumulator is restarted every chunk and
                                    chunk sums are added in fp32 round-to-nearest */
-    GEMM_OPT_TC_PAIR = 5        /* tensor-core tiles: 0 choose (default: pairs when M > 128), 1 one CTA per
+    GEMM_OPT_TC_PAIR = 5,       /* tensor-core tiles: 0 choose (default: pairs when M > 128), 1 one CTA per
                                    128x256 tile, 2 a pair of CTAs (cluster of two) per 256x256 tile */
+    GEMM_OPT_TEST_STALL = 6     /* test hook for failure detection, 0 (default) or 1: the kernels with
+                                   bounded waits (tensor-core GEMMs, TMA skinny GEMM) first wait on a
+                                   barrier nothing arrives on; the wait runs out after the wait limit, the
+                                   kernel drains its copies and MMAs, frees its tensor memory, returns,
+                                   and gemm_get_device_status reports GEMM_ERR_DEVICE_TIMEOUT.  C is not
+                                   written.  No fault, trap or unbounded wait is involved. */
 } gemm_option_t;
 int gemm_set_option(gemm_handle_t h, int option, int64_t value);
 

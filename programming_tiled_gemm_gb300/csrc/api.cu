@@ -27,6 +27,7 @@ struct gemm_ctx {
     int opt_split_k = 0;
     int opt_tc_chunk = 0;  // tensor-core accumulation chunk in 64-wide k-blocks (0 = default)
     int opt_tc_pair = 0;   // tensor-core tile: 0 choose, 1 single CTA, 2 CTA pair
+    int opt_test_stall = 0;  // test hook: kernels with bounded waits let one wait run out
     uint64_t wait_limit_ns = 2000000000ull;
     int64_t launches = 0;  // kernels launched through this handle
 };
@@ -111,7 +112,8 @@ int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)
     cudaError_t e;
     int n = 0;
     if (kernel == 4)
-        e = launch_skinny_tma(a, split, h->workspace, h->num_sms, h->d_status, h->wait_limit_ns, stream, &n);
+        e = launch_skinny_tma(a, split, h->workspace, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall,
+                              stream, &n);
     else if (kernel == 3)
         e = launch_skinny(a, split, h->workspace, h->num_sms, stream, &n);
     else
@@ -186,6 +188,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
         h->opt_tc_pair = (int)value;
         return GEMM_OK;
+    case GEMM_OPT_TEST_STALL:
+        if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+        h->opt_test_stall = (int)value;
+        return GEMM_OK;
     case GEMM_OPT_WAIT_LIMIT_US:
         if (value < 0 || value > 60000000) return GEMM_ERR_INVALID_ARG;
         h->wait_limit_ns = value == 0 ? 2000000000ull : (uint64_t)value * 1000ull;
@@ -215,7 +221,7 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, in
         F32Args a{M, N, K, static_cast<const float*>(A), lda, static_cast<const float*>(B), ldb, C, ldc};
         return run_f32(h, a, s);
     }
-    TcArgs t{M, N, K, A, lda, B, ldb, C, ldc, dtype == GEMM_BF16 ? 1 : 0};
+    TcArgs t{M, N, K, A, lda, B, ldb, C, ldc, dtype == GEMM_BF16 ? 1 : 0, h->opt_test_stall};
     int n = 0;
     int rc2 = launch_tc_gemm(t, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_tc_chunk, h->opt_tc_pair, s, &n);
     h->launches += n;

@@ -41,7 +41,7 @@ cudaError_t launch_skinny(const F32Args& a, int split, float* workspace, int num
 bool skinny_tma_supported(const F32Args& a);
 int skinny_tma_auto_split(const F32Args& a, int num_sms);
 cudaError_t launch_skinny_tma(const F32Args& a, int split, float* workspace, int num_sms, int* dev_status,
-                              uint64_t limit_ns, cudaStream_t stream, int* launches);
+                              uint64_t limit_ns, int test_stall, cudaStream_t stream, int* launches);
 
 // Fixed-order split-K reduction: C[m][n] = sum_{s=0..split-1} ws[s][m][n].
 cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t N, float* C,
@@ -73,7 +73,8 @@ struct TcArgs {
     int64_t ldb;
     float* C;
     int64_t ldc;
-    int is_bf16;  // 1 = bf16, 0 = fp16
+    int is_bf16;     // 1 = bf16, 0 = fp16
+    int test_stall;  // test hook: make a bounded wait run out (exercises the timeout path)
 };
 // Returns GEMM_OK or a negative gemm_status_t.
 // kc_blocks: 64-wide k-blocks per accumulation chunk (0 = default 16).

@@ -112,6 +112,7 @@ struct StParams {
     int vec_out;
     int* status;
     uint64_t limit_ns;
+    int test_stall;  // test hook: consumers first wait on a barrier nothing arrives on
 };
 
 template <int MR, int COLW, int MSPLIT>
@@ -131,7 +132,8 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ST_STAGES * (ST_B_STAGE_BYTES + SM::A_STAGE_BYTES));
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + ST_STAGES;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * ST_STAGES);
+    uint64_t* never_bar = bars + 2 * ST_STAGES;  // never completes (test hook)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * ST_STAGES + 1);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -142,6 +144,7 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
             st_mbar_init(st_smem_u32(&full_bar[s]), 1);
             st_mbar_init(st_smem_u32(&empty_bar[s]), CONSUMER_WARPS);
         }
+        st_mbar_init(st_smem_u32(never_bar), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
@@ -222,7 +225,18 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
         const int m_base = mg * RT;
         int stage = 0;
         uint32_t phase = 0;
-        for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+        int item_first = blockIdx.x;
+        if (p.test_stall) {
+            // test hook: a wait nothing will satisfy runs out and takes the abort path
+            bool got = st_mbar_wait(st_smem_u32(never_bar), 0, p.limit_ns, abort_flag);
+            got = __all_sync(0xffffffffu, got);
+            if (!got && lane == 0) {
+                atomicCAS(p.status, 0, kDevTimeoutMma);
+                *abort_flag = 1;
+            }
+            item_first = p.num_items;
+        }
+        for (int item = item_first; item < p.num_items; item += gridDim.x) {
             const int cb = item % p.col_blocks, sp = item / p.col_blocks;
             const int64_t kbeg = (int64_t)sp * p.k_per_split;
             const int64_t kend = min(a.K, kbeg + p.k_per_split);
@@ -317,7 +331,7 @@ PFN_cuTensorMapEncodeTiled_v12000 st_encoder()
 
 template <int MR, int COLW, int MSPLIT>
 cudaError_t launch_mr_tma(const F32Args& a, int split, float* ws, int num_sms, int* dev_status,
-                          uint64_t limit_ns, cudaStream_t stream, int* launches)
+                          uint64_t limit_ns, int test_stall, cudaStream_t stream, int* launches)
 {
     // B as a [K][N] fp32 tensor, box 256 columns x 8 rows, no swizzle, zero fill outside
     CUtensorMap tmB;
@@ -348,6 +362,7 @@ cudaError_t launch_mr_tma(const F32Args& a, int split, float* ws, int num_sms, i
         p.vec_out = (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0;
     p.status = dev_status;
     p.limit_ns = limit_ns;
+    p.test_stall = test_stall;
     constexpr int smem = StCfg<MR, COLW, MSPLIT>::BYTES;
     constexpr int threads = StCfg<MR, COLW, MSPLIT>::THREADS;
     auto kern = skinny_tma_kernel<MR, COLW, MSPLIT>;
@@ -401,11 +416,13 @@ int skinny_tma_auto_split(const F32Args& a, int num_sms)
 }
 
 cudaError_t launch_skinny_tma(const F32Args& a, int split, float* ws, int num_sms, int* dev_status,
-                              uint64_t limit_ns, cudaStream_t stream, int* launches)
+                              uint64_t limit_ns, int test_stall, cudaStream_t stream, int* launches)
 {
     if (split < 1) split = 1;
-    if (a.M <= 16) return launch_mr_tma<16, 8, 1>(a, split, ws, num_sms, dev_status, limit_ns, stream, launches);
-    if (a.M <= 32) return launch_mr_tma<32, 6, 2>(a, split, ws, num_sms, dev_status, limit_ns, stream, launches);
+    if (a.M <= 16)
+        return launch_mr_tma<16, 8, 1>(a, split, ws, num_sms, dev_status, limit_ns, test_stall, stream, launches);
+    if (a.M <= 32)
+        return launch_mr_tma<32, 6, 2>(a, split, ws, num_sms, dev_status, limit_ns, test_stall, stream, launches);
     return cudaErrorInvalidValue;
 }
 

@@ -239,6 +239,7 @@ struct TcParams {
     int vec_store;
     int* status;
     uint64_t limit_ns;
+    int test_stall;  // test hook: the epilogue first waits on a barrier nothing arrives on
 };
 
 __device__ __forceinline__ void record_error(int* status, int code, volatile int* abort_flag)
@@ -262,7 +263,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint64_t* tfull_bar = bars + 2 * STAGES;      // [2] chunk accumulator complete
     uint64_t* tempty_bar = bars + 2 * STAGES + 2; // [2] chunk accumulator read by the epilogue
     uint64_t* drain_bar = bars + 2 * STAGES + 4;  // MMA issuer's final completion check
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    uint64_t* never_bar = bars + 2 * STAGES + 5;  // never completes (test hook)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x / 32;
@@ -278,6 +280,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             mbar_init(smem_u32(&tempty_bar[a]), EPI_WARPS);  // one arrival per epilogue warp
         }
         mbar_init(smem_u32(drain_bar), 1);
+        mbar_init(smem_u32(never_bar), 1);
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tensormap(&tmA);
@@ -393,7 +396,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int buf = 0;
         uint32_t buf_phase = 0;
         float tot[EPI_COLS];
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        int t_first = blockIdx.x;
+        if (p.test_stall) {
+            // test hook: a wait nothing will satisfy runs out and takes the abort path
+            bool ok = mbar_wait(smem_u32(never_bar), 0, p.limit_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok && lane == 0) record_error(p.status, kDevTimeoutEpilogue, abort_flag);
+            t_first = p.num_tiles;
+        }
+        for (int t = t_first; t < p.num_tiles; t += gridDim.x) {
             bool ok = true;
             for (int ch = 0; ch < p.nchunks; ++ch) {
                 ok = !*abort_flag && mbar_wait(smem_u32(&tfull_bar[buf]), buf_phase, p.limit_ns);
@@ -592,7 +603,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     uint64_t* tfull_bar = bars + 2 * P_STAGES;       // [2] (both CTAs, multicast)
     uint64_t* tempty_bar = bars + 2 * P_STAGES + 2;  // [2] (used in the even CTA)
     uint64_t* drain_bar = bars + 2 * P_STAGES + 4;   // (both CTAs, multicast)
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 5);
+    uint64_t* never_bar = bars + 2 * P_STAGES + 5;   // never completes (test hook)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x / 32;
@@ -611,6 +623,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             mbar_init(smem_u32(&tempty_bar[a]), 2 * EPI_WARPS);  // epilogue warps of both CTAs
         }
         mbar_init(smem_u32(drain_bar), 1);
+        mbar_init(smem_u32(never_bar), 1);
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tensormap(&tmA);
@@ -726,7 +739,16 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int buf = 0;
         uint32_t buf_phase = 0;
         float tot[EPI_COLS];
-        for (int t = pair; t < p.num_tiles; t += npairs) {
+        int t_first = pair;
+        if (p.test_stall) {
+            // test hook: a wait nothing will satisfy runs out and takes the abort path
+            bool ok = mbar_wait_cluster(smem_u32(never_bar), 0, p.limit_ns, nullptr);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok && lane == 0) record_error(p.status, kDevTimeoutEpilogue, abort_flag);
+            aborted = true;
+            t_first = p.num_tiles;
+        }
+        for (int t = t_first; t < p.num_tiles; t += npairs) {
             bool ok = true;
             for (int ch = 0; ch < p.nchunks; ++ch) {
                 ok = mbar_wait_cluster(smem_u32(&tfull_bar[buf]), buf_phase, p.limit_ns, abort_flag);
@@ -863,6 +885,7 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.vec_store = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && (a.ldc % 4 == 0);
     p.status = dev_status;
     p.limit_ns = wait_limit_ns;
+    p.test_stall = a.test_stall;
     // CTA pairs: 256 x 256 tiles on clusters of two; single CTAs: 128 x 256 tiles
     const bool use_pair = (pair_mode == 2) || (pair_mode == 0 && a.M > BM && num_sms >= 2);
     if (use_pair) {
