@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--ref-budget-s", type=float, default=150.0,
+                    help="--impl reference: target wall time of warm-up plus timed steps")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     a.steps = max(a.steps, 1)
@@ -138,6 +140,23 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(clocks) if clocks else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(busy),
                 "power_w_max": max((num(r[3]) or 0) for r in rows)}
+
+
+def reduce_max(value: float, dist_mod, device) -> float:
+    """Max of a per-rank scalar over the process group (identity without one)."""
+    if dist_mod is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(flops_per_step: float, ms_local: float, world: int, dist_mod, device):
+    """Whole-job throughput of `world` replicas: every rank does `flops_per_step` per step
+    and the step time is the slowest rank's.  Returns (TFLOP/s, ms per step)."""
+    ms = reduce_max(ms_local, dist_mod, device)
+    return world * flops_per_step / (ms * 1e-3) / 1e12, ms
 
 
 def clocks_rejected(c) -> bool:
@@ -256,13 +275,8 @@ def run_ours(args, rank, world, local_rank):
     if lib.device_status() != 0:
         raise RuntimeError("device status error in the timed region")
 
-    ms_step = statistics.mean(step_ms)
-    if pg:
-        t = torch.tensor([ms_step], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_step = float(t.item())
     flops_step = sum(op[0].flops for op in ops)
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value, ms_step = aggregate(flops_step, statistics.mean(step_ms), world, pg, dev)
 
     peaks, peak_src = load_peaks()
     sm_mhz = clocks.get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
@@ -409,11 +423,7 @@ def measure_e2e(lib, ops, args, dev, world, pg, reps=None):
     for _ in range(n):
         for w, A, B, C in host:
             lib.matmul_host(A, B, out=C)
-    dt = (time.perf_counter() - t0) / n
-    if pg:
-        t = torch.tensor([dt], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        dt = float(t.item())
+    dt = reduce_max((time.perf_counter() - t0) / n, pg, dev)
     flops = sum(w.flops for w, *_ in host)
     return {"value": round(world * flops / dt / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(dt * 1e3, 3), "steps": n,
@@ -467,7 +477,7 @@ def run_reference(args, rank, world):
     f0, t0 = oracle_sample(ops_cpu, [4] * len(ops_cpu))
     rate = f0 / max(t0, 1e-6)
     per_row = sum(2 * w.N * w.K for w, *_ in ops_cpu)
-    budget = 150.0 / (args.steps + args.warmup)
+    budget = args.ref_budget_s / (args.steps + args.warmup)
     rows = int(max(1, min(min(w.M for w, *_ in ops_cpu), budget * rate / per_row)))
     for _ in range(args.warmup):
         oracle_sample(ops_cpu, [rows] * len(ops_cpu))
