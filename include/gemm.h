@@ -85,9 +85,15 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
              const void* A, int64_t lda, const void* B, int64_t ldb,
              float* C, int64_t ldc, gemm_dtype_t dtype, void* stream);
 
-/* The same product with A, B and C in HOST memory (pageable or pinned).  Copies A and
- * B into handle-owned device buffers on `stream`, runs gemm_run, copies C back and
- * synchronises `stream` before returning.  Leading dimensions as in gemm_run. */
+/* The same product with A, B and C in HOST memory (pageable or pinned).  A and B are
+ * copied into handle-owned device buffers and C is copied back, on two internal
+ * streams ordered after the work already queued on `stream`; the product runs on
+ * `stream`.  Large products are pipelined over row chunks (a multiple of 256 rows;
+ * up to 8 chunks of >= 1024 rows for 16-bit inputs, 2 chunks of >= 2048 rows for fp32):
+ * A chunk i+1 travels while chunk i computes, and C chunk i travels back while chunk
+ * i+1 computes.  Overlap needs
+ * pinned host memory; pageable memory is copied through the driver's staging.
+ * Returns after `stream` has been synchronised.  Leading dimensions as in gemm_run. */
 int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                   const void* A, int64_t lda, const void* B, int64_t ldb,
                   float* C, int64_t ldc, gemm_dtype_t dtype, void* stream);

@@ -30,6 +30,11 @@ struct gemm_ctx {
     int opt_test_stall = 0;  // test hook: kernels with bounded waits let one wait run out
     uint64_t wait_limit_ns = 2000000000ull;
     int64_t launches = 0;  // kernels launched through this handle
+    // gemm_run_host pipeline: copy-in and copy-out streams and their events
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    static constexpr int kMaxChunks = 8;
+    cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_a[kMaxChunks] = {}, ev_c[kMaxChunks] = {};
 };
 
 namespace {
@@ -160,6 +165,14 @@ int gemm_destroy(gemm_handle_t h)
     if (!h) return GEMM_OK;
     DeviceGuard g(h->device);
     cudaDeviceSynchronize();
+    if (h->s_in) cudaStreamDestroy(h->s_in);
+    if (h->s_out) cudaStreamDestroy(h->s_out);
+    if (h->ev_start) cudaEventDestroy(h->ev_start);
+    if (h->ev_done) cudaEventDestroy(h->ev_done);
+    for (int i = 0; i < gemm_ctx::kMaxChunks; ++i) {
+        if (h->ev_a[i]) cudaEventDestroy(h->ev_a[i]);
+        if (h->ev_c[i]) cudaEventDestroy(h->ev_c[i]);
+    }
     if (h->d_status) cudaFree(h->d_status);
     if (h->workspace) cudaFree(h->workspace);
     for (int i = 0; i < 3; ++i)
@@ -228,8 +241,38 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, in
     return rc2;
 }
 
-int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                  const void* B, int64_t ldb, float* C, int64_t ldc, gemm_dtype_t dtype, void* stream)
+}  // extern "C"
+
+namespace {
+
+// Row-pitched copy; one contiguous copy when both sides are dense.
+cudaError_t copy_rows(void* dst, size_t dpitch, const void* src, size_t spitch, size_t width, size_t rows,
+                      cudaMemcpyKind kind, cudaStream_t s)
+{
+    if (rows == 0 || width == 0) return cudaSuccess;
+    if (dpitch == width && spitch == width) return cudaMemcpyAsync(dst, src, width * rows, kind, s);
+    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, s);
+}
+
+int ensure_pipeline(gemm_handle_t h)
+{
+    if (h->s_in) return GEMM_OK;
+    if (cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    for (int i = 0; i < gemm_ctx::kMaxChunks; ++i)
+        if (cudaEventCreateWithFlags(&h->ev_a[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h->ev_c[i], cudaEventDisableTiming) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                             const void* B, int64_t ldb, float* C, int64_t ldc, gemm_dtype_t dtype, void* stream)
 {
     int rc = check_common(h, M, N, K, A, lda, B, ldb, C, ldc, (int)dtype);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
@@ -244,20 +287,57 @@ int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* 
         if ((rc = ensure_buffer(&h->stage[1], &h->stage_bytes[1], (size_t)K * ldb_d * es)) != GEMM_OK) return rc;
     }
     if ((rc = ensure_buffer(&h->stage[2], &h->stage_bytes[2], (size_t)M * ldc_d * 4)) != GEMM_OK) return rc;
-    if (K > 0) {
-        if (cudaMemcpy2DAsync(h->stage[0], lda_d * es, A, lda * es, K * es, M, cudaMemcpyHostToDevice, s) !=
-                cudaSuccess ||
-            cudaMemcpy2DAsync(h->stage[1], ldb_d * es, B, ldb * es, N * es, K, cudaMemcpyHostToDevice, s) !=
-                cudaSuccess)
+    if ((rc = ensure_pipeline(h)) != GEMM_OK) return rc;
+
+    // Pipeline over row chunks of A and C: B and A chunk i go in on s_in, the product of
+    // chunk i runs on the caller's stream once its rows are in, and C chunk i comes back
+    // on s_out while later chunks still compute.  16-bit inputs are transfer-bound (the
+    // tensor cores outrun a ~200 GB/s host link), so they take up to 8 chunks of >= 1024
+    // rows; fp32 is compute-bound, so 2 chunks of >= 2048 rows keep its launches full.
+    int64_t chunk = M;
+    int nchunks = 1;
+    const int64_t min_rows = (dtype == GEMM_F32) ? 2048 : 1024;
+    const int max_chunks = (dtype == GEMM_F32) ? 2 : gemm_ctx::kMaxChunks;
+    if (K > 0 && M >= 2 * min_rows) {
+        nchunks = (int)(M / min_rows);
+        if (nchunks > max_chunks) nchunks = max_chunks;
+        chunk = ((M + nchunks - 1) / nchunks + 255) / 256 * 256;
+        nchunks = (int)((M + chunk - 1) / chunk);
+    }
+    uint8_t* Ad = static_cast<uint8_t*>(h->stage[0]);
+    float* Cd = static_cast<float*>(h->stage[2]);
+    const uint8_t* Ah = static_cast<const uint8_t*>(A);
+    float* Ch = C;
+    if (cudaEventRecord(h->ev_start, s) != cudaSuccess || cudaStreamWaitEvent(h->s_in, h->ev_start, 0) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (K > 0 && copy_rows(h->stage[1], ldb_d * es, B, ldb * es, N * es, K, cudaMemcpyHostToDevice, h->s_in) !=
+                     cudaSuccess)
+        return GEMM_ERR_CUDA;
+    for (int i = 0; i < nchunks; ++i) {
+        const int64_t m0 = i * chunk, rows = (M - m0) < chunk ? (M - m0) : chunk;
+        if (K > 0 && copy_rows(Ad + m0 * lda_d * es, lda_d * es, Ah + m0 * lda * es, lda * es, K * es, rows,
+                               cudaMemcpyHostToDevice, h->s_in) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaEventRecord(h->ev_a[i], h->s_in) != cudaSuccess) return GEMM_ERR_CUDA;
+    }
+    for (int i = 0; i < nchunks; ++i) {
+        const int64_t m0 = i * chunk, rows = (M - m0) < chunk ? (M - m0) : chunk;
+        if (cudaStreamWaitEvent(s, h->ev_a[i], 0) != cudaSuccess) return GEMM_ERR_CUDA;
+        rc = gemm_run(h, rows, N, K, Ad + m0 * lda_d * es, lda_d, h->stage[1], ldb_d, Cd + m0 * ldc_d, ldc_d, dtype,
+                      stream);
+        if (rc != GEMM_OK) return rc;
+        if (cudaEventRecord(h->ev_c[i], s) != cudaSuccess || cudaStreamWaitEvent(h->s_out, h->ev_c[i], 0) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (copy_rows(Ch + m0 * ldc, ldc * 4, Cd + m0 * ldc_d, ldc_d * 4, N * 4, rows, cudaMemcpyDeviceToHost,
+                      h->s_out) != cudaSuccess)
             return GEMM_ERR_CUDA;
     }
-    rc = gemm_run(h, M, N, K, h->stage[0], lda_d, h->stage[1], ldb_d, static_cast<float*>(h->stage[2]), ldc_d,
-                  dtype, stream);
-    if (rc != GEMM_OK) return rc;
-    if (cudaMemcpy2DAsync(C, ldc * 4, h->stage[2], ldc_d * 4, N * 4, M, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (cudaEventRecord(h->ev_done, h->s_out) != cudaSuccess || cudaStreamWaitEvent(s, h->ev_done, 0) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return from_cuda(cudaStreamSynchronize(s));
 }
+
+extern "C" {
 
 int conv4d_im2col(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4],
                   const int64_t k_dims[4], float* col, void* stream)

@@ -176,3 +176,22 @@ def test_config_8192_sampled_and_freivalds(lib):
         rhs = A64 @ (B64 @ x)
         bound = tol * math.sqrt(w.N) * 6 + 1e-9 * np.abs(A64) @ np.abs(B64 @ x)
         assert np.all(np.abs(lhs - rhs) <= bound)
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_host_entry_point_pipelined_chunks(lib, pinned, dtype):
+    """M >= 4096 takes the chunked copy/compute pipeline; rows not a multiple of the chunk,
+    a padded host leading dimension for A and C, integer inputs: exact."""
+    M, N, K = 4352 + 3, 264, 72
+    A, B = si.integer_copy(M, N, K, seed=44, dtype=dtype)
+    tdt = A.dtype
+    Abig = torch.zeros((M, K + 8), dtype=tdt)
+    Abig[:, :K] = A
+    Cbig = torch.full((M, N + 5), -3.0)
+    if pinned:
+        Abig, Cbig, B = Abig.pin_memory(), Cbig.pin_memory(), B.pin_memory()
+    lib.matmul_host(Abig[:, :K], B, out=Cbig[:, :N])
+    ref = oracle.gemm(A.float().numpy(), B.float().numpy())
+    assert np.array_equal(Cbig[:, :N].double().numpy(), ref)
+    assert torch.all(Cbig[:, N:] == -3.0)
