@@ -53,9 +53,12 @@ def _load():
         i64, p = ctypes.c_int64, ctypes.c_void_p
         lib.oracle_gemm.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, ctypes.c_int]
         lib.oracle_gemm_entries.argtypes = [i64, i64, i64, p, i64, p, i64, i64, i64, p, p, p, ctypes.c_int]
+        d = ctypes.c_double
+        lib.oracle_gemm_general.argtypes = [i64, i64, i64, d, p, i64, p, i64, d, p, i64, p, i64, ctypes.c_int]
         lib.oracle_conv4d_direct.argtypes = [i64, p, i64, p, p, p, p, ctypes.c_int]
         lib.oracle_im2col4d.argtypes = [i64, p, p, p, p]
-        for f in (lib.oracle_gemm, lib.oracle_gemm_entries, lib.oracle_conv4d_direct, lib.oracle_im2col4d):
+        for f in (lib.oracle_gemm, lib.oracle_gemm_entries, lib.oracle_gemm_general, lib.oracle_conv4d_direct,
+                  lib.oracle_im2col4d):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -106,6 +109,34 @@ def gemm(A: np.ndarray, B: np.ndarray, nthreads: int | None = None) -> np.ndarra
     if rc != 0:
         raise RuntimeError("oracle_gemm rejected its arguments (rc=%d)" % rc)
     return C
+
+
+def gemm_general(alpha: float, A: np.ndarray, B: np.ndarray, beta: float = 0.0, C: np.ndarray | None = None,
+                 nthreads: int | None = None) -> np.ndarray:
+    """D = alpha * (A @ B) + beta * C in fp64 ("generalised" GEMM; C unread when beta == 0).
+
+    C, when given, is converted to float64 (exact for fp32 and bf16 values)."""
+    A, B = _f32(A), _f32(B)
+    M, K = A.shape
+    N = B.shape[1]
+    if B.shape[0] != K:
+        raise ValueError("inner dimensions differ")
+    lda = _check_2d(A, M, K, "A") if M and K else max(K, 1)
+    ldb = _check_2d(B, K, N, "B") if K and N else max(N, 1)
+    D = np.empty((M, N), dtype=np.float64)
+    if M == 0 or N == 0:
+        return D
+    Cp = None
+    if beta != 0.0:
+        if C is None or C.shape != (M, N):
+            raise ValueError("beta != 0 needs C of shape (M, N)")
+        Cp = np.ascontiguousarray(C, dtype=np.float64)
+    rc = _load().oracle_gemm_general(M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb, float(beta),
+                                     _ptr(Cp) if Cp is not None else None, N, _ptr(D), N,
+                                     nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_gemm_general rejected its arguments (rc=%d)" % rc)
+    return D
 
 
 def gemm_entries(A: np.ndarray, B: np.ndarray, rows, cols, nthreads: int | None = None,
@@ -180,4 +211,4 @@ def im2col4d(x: np.ndarray, ks) -> np.ndarray:
     return col
 
 
-__all__ = ["build", "gemm", "gemm_entries", "conv4d_direct", "im2col4d", "default_threads"]
+__all__ = ["build", "gemm", "gemm_general", "gemm_entries", "conv4d_direct", "im2col4d", "default_threads"]

@@ -21,6 +21,12 @@
  *       additions 0 + A[i][0]B[0][j] + A[i][1]B[1][j] + ... in that order, so the
  *       result is bit-identical to the i, j, k nesting.
  *
+ *   oracle_gemm_general  the "generalised" product of the same page, section "Generalised
+ *       matrix multiplication GEMM": a weighted product added to a weighted accumulator,
+ *         D[i][j] = alpha * (sum_k A[i][k] * B[k][j]) + beta * C[i][j],
+ *       with the sum exactly as in oracle_gemm and C not read when beta == 0 (the usual
+ *       BLAS convention); double precision throughout, each operation rounded once.
+ *
  *   oracle_gemm_entries  the same sum for a list of (i, j) pairs, with B given by
  *       an arbitrary element stride pair so a transposed copy can be streamed.
  *
@@ -136,6 +142,23 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
     if (ldc < N || (K > 0 && (lda < K || ldb < N))) return -1;
     gemm_ctx_t g = {N, K, A, lda, B, ldb, C, ldc};
     return parallel_rows(gemm_rows, &g, M, nthreads);
+}
+
+int oracle_gemm_general(int64_t M, int64_t N, int64_t K, double alpha, const float* A, int64_t lda,
+                        const float* B, int64_t ldb, double beta, const double* C, int64_t ldc, double* D,
+                        int64_t ldd, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (M == 0 || N == 0) return 0;
+    if (beta != 0.0 && (!C || ldc < N)) return -1;
+    int rc = oracle_gemm(M, N, K, A, lda, B, ldb, D, ldd, nthreads);
+    if (rc != 0) return rc;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            const double prod = alpha * D[i * ldd + j];
+            D[i * ldd + j] = (beta != 0.0) ? prod + beta * C[i * ldc + j] : prod;
+        }
+    return 0;
 }
 
 typedef struct {

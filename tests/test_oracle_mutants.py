@@ -33,6 +33,13 @@ GEMM_PINS = [
     lambda: pins.test_sum_runs_over_k_ascending(),
     lambda: pins.test_entries_equal_full_product_bit_for_bit(),
 ]
+GENERAL_PINS = [
+    lambda: pins.test_general_with_alpha_one_beta_zero_is_the_product(),
+    lambda: pins.test_general_beta_zero_never_reads_C(),
+    lambda: pins.test_general_zero_product_scales_the_accumulator(),
+    lambda: pins.test_general_closed_form_with_dyadic_weights(),
+    lambda: pins.test_general_matches_numpy_float64(),
+]
 CONV_PINS = [
     lambda: pins.test_conv_all_ones_counts_taps(),
     lambda: pins.test_conv_delta_filter_is_a_shifted_crop(),
@@ -54,6 +61,11 @@ MUTANTS = [
     ("no_zero_init", "for (int64_t j = 0; j < g->N; ++j) c[j] = 0.0;", "", GEMM_PINS),
     ("entries_drop_last", "for (int64_t k = 0; k < e->K; ++k) {", "for (int64_t k = 0; k + 1 < e->K; ++k) {",
      GEMM_PINS),
+    ("general_beta_times_alpha", "prod + beta * C[i * ldc + j]", "prod + alpha * C[i * ldc + j]", GENERAL_PINS),
+    ("general_no_alpha", "const double prod = alpha * D[i * ldd + j];", "const double prod = D[i * ldd + j];",
+     GENERAL_PINS),
+    ("general_reads_C_always", "(beta != 0.0) ? prod + beta * C[i * ldc + j] : prod", "prod + beta * C[i * ldc + j]",
+     GENERAL_PINS),
     ("conv_flipped_filter", "* R1 + r1) * R2 + r2) * R3 + r3;", "* R1 + r1) * R2 + r2) * R3 + (R3 - 1 - r3);",
      CONV_PINS),
     ("conv_drop_channel", "for (int64_t ci = 0; ci < c->Cin; ++ci)", "for (int64_t ci = 1; ci < c->Cin; ++ci)",
@@ -84,7 +96,7 @@ import oracle
 import test_oracle_mutants as m
 oracle._load()
 mutant = ctypes.CDLL({so!r})
-for fn in ("oracle_gemm", "oracle_gemm_entries", "oracle_conv4d_direct", "oracle_im2col4d"):
+for fn in ("oracle_gemm", "oracle_gemm_entries", "oracle_gemm_general", "oracle_conv4d_direct", "oracle_im2col4d"):
     getattr(mutant, fn).argtypes = getattr(oracle._lib, fn).argtypes
     getattr(mutant, fn).restype = ctypes.c_int
 oracle._lib = mutant
@@ -116,5 +128,5 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new, checks):
 
 
 def test_unmutated_oracle_passes_every_pin():
-    for check in GEMM_PINS + CONV_PINS:
+    for check in GEMM_PINS + GENERAL_PINS + CONV_PINS:
         check()

@@ -186,6 +186,46 @@ def test_rejects_mismatched_shapes():
         oracle.gemm(np.zeros((3, 4)), np.zeros((4, 2)))
 
 
+# ----------------------------------------------------------- generalised GEMM pins
+
+def test_general_with_alpha_one_beta_zero_is_the_product():
+    A = f32(RNG.uniform(-1, 1, (13, 21)))
+    B = f32(RNG.uniform(-1, 1, (21, 8)))
+    assert np.array_equal(oracle.gemm_general(1.0, A, B), oracle.gemm(A, B))
+
+
+def test_general_beta_zero_never_reads_C():
+    A = f32(np.ones((3, 4)))
+    B = f32(np.ones((4, 5)))
+    C = np.full((3, 5), np.nan)
+    assert np.array_equal(oracle.gemm_general(2.0, A, B, 0.0, C), np.full((3, 5), 8.0))
+
+
+def test_general_zero_product_scales_the_accumulator():
+    # A = 0: D = beta * C exactly
+    C = RNG.uniform(-1, 1, (6, 7))
+    D = oracle.gemm_general(3.0, f32(np.zeros((6, 5))), f32(RNG.uniform(-1, 1, (5, 7))), -0.25, C)
+    assert np.array_equal(D, -0.25 * C)
+
+
+def test_general_closed_form_with_dyadic_weights():
+    # A = all ones (M x K), B = all ones (K x N), C = i - j: D = alpha*K + beta*(i - j)
+    M, K, N = 9, 12, 7
+    alpha, beta = 0.5, -2.0
+    C = np.subtract.outer(np.arange(M), np.arange(N)).astype(np.float64)
+    D = oracle.gemm_general(alpha, f32(np.ones((M, K))), f32(np.ones((K, N))), beta, C)
+    assert np.array_equal(D, alpha * K + beta * C)
+
+
+def test_general_matches_numpy_float64():
+    A = f32(RNG.uniform(-1, 1, (17, 33)))
+    B = f32(RNG.uniform(-1, 1, (33, 11)))
+    C = RNG.uniform(-1, 1, (17, 11))
+    D = oracle.gemm_general(1.75, A, B, 0.5, C)
+    ref = 1.75 * (A.astype(np.float64) @ B.astype(np.float64)) + 0.5 * C
+    assert np.allclose(D, ref, rtol=0, atol=1e-12)
+
+
 # ------------------------------------------------------------------ convolution pins
 
 def conv_case(cin, ins, cout, ks, seed=7):
