@@ -85,6 +85,23 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
              const void* A, int64_t lda, const void* B, int64_t ldb,
              float* C, int64_t ldc, gemm_dtype_t dtype, void* stream);
 
+/* The generalised product of "Learning to develop for GPU with GEMM as the example",
+ * section "Generalised matrix multiplication GEMM" (a weighted product added to a
+ * weighted accumulator):
+ *     C = alpha * (A . B) + beta * C,
+ * with C stored as c_dtype (GEMM_F32, GEMM_BF16 or GEMM_F16; rounded to nearest even)
+ * and read only when beta != 0 (the BLAS convention: with beta == 0, C may hold
+ * anything, NaN included).  The product accumulates in fp32 as in gemm_run; the
+ * epilogue computes alpha * p in fp32, then fma(beta, c, .) in fp32, then converts.
+ * Tensor-core products (bf16 / fp16 inputs) apply it as they store C; fp32 inputs
+ * store their fp32 product in a handle-owned buffer (M x N floats, grown on demand)
+ * and apply it in one more pass.  C must be aligned to its element size; other
+ * arguments and errors as in gemm_run.  gemm_run is this call with alpha = 1,
+ * beta = 0, c_dtype = GEMM_F32. */
+int gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha,
+                const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
+                void* C, int64_t ldc, gemm_dtype_t ab_dtype, gemm_dtype_t c_dtype, void* stream);
+
 /* The same product with A, B and C in HOST memory (pageable or pinned).  A and B are
  * copied into handle-owned device buffers and C is copied back, on two internal
  * streams ordered after the work already queued on `stream`; the product runs on

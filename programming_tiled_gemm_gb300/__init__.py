@@ -24,7 +24,8 @@ GEMM_OPT_F32_KERNEL, GEMM_OPT_SPLIT_K, GEMM_OPT_WAIT_LIMIT_US, GEMM_OPT_TC_CHUNK
 GEMM_OPT_TEST_STALL = 6
 
 # Every symbol include/gemm.h declares (the ABI test checks the library exports them).
-EXPORTS = ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "conv4d_im2col", "conv4d_forward",
+EXPORTS = ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host", "conv4d_im2col",
+           "conv4d_forward",
            "gemm_get_device_status", "gemm_set_option", "gemm_launch_count", "gemm_status_string",
            "gemm_run_f32_skinny_noalloc"]
 
@@ -44,6 +45,8 @@ def _load():
     lib.gemm_destroy.argtypes = [p]
     lib.gemm_run.argtypes = [p, i64, i64, i64, p, i64, p, i64, p, i64, i32, p]
     lib.gemm_run_host.argtypes = [p, i64, i64, i64, p, i64, p, i64, p, i64, i32, p]
+    f32 = ctypes.c_float
+    lib.gemm_run_ex.argtypes = [p, i64, i64, i64, f32, p, i64, p, i64, f32, p, i64, i32, i32, p]
     lib.conv4d_im2col.argtypes = [p, p, i64, ctypes.POINTER(i64), ctypes.POINTER(i64), p, p]
     lib.conv4d_forward.argtypes = [p, p, i64, ctypes.POINTER(i64), p, i64, ctypes.POINTER(i64), p, i64, p]
     lib.gemm_get_device_status.argtypes = [p, p]
@@ -83,6 +86,10 @@ def gemm_destroy(h: int) -> int:
 
 def gemm_run(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream=0) -> int:
     return _lib.gemm_run(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream)
+
+
+def gemm_run_ex(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ab_dtype, c_dtype, stream=0) -> int:
+    return _lib.gemm_run_ex(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ab_dtype, c_dtype, stream)
 
 
 def gemm_run_host(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream=0) -> int:
@@ -166,8 +173,9 @@ class Gemm:
         if rc != GEMM_OK:
             raise GemmError(rc, "gemm_set_option")
 
-    def matmul(self, A, B, out=None, stream=None):
-        """out[M, N] (fp32) = A[M, K] @ B[K, N]; A, B fp32 / bf16 / fp16 CUDA tensors."""
+    def matmul(self, A, B, out=None, stream=None, alpha=1.0, beta=0.0, out_dtype=None):
+        """out[M, N] = alpha * A[M, K] @ B[K, N] + beta * out; A, B fp32 / bf16 / fp16 CUDA
+        tensors; out fp32 (default) or bf16 / fp16; out is read only when beta != 0."""
         import torch
         if A.dtype != B.dtype:
             raise TypeError("A and B must have the same dtype")
@@ -176,11 +184,17 @@ class Gemm:
         if K2 != K:
             raise ValueError("inner dimensions differ")
         if out is None:
-            out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+            if beta != 0.0:
+                raise ValueError("beta != 0 needs an existing out")
+            out = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
         lda, ldb, ldc = _row_major_2d(A, "A"), _row_major_2d(B, "B"), _row_major_2d(out, "out")
         s = torch.cuda.current_stream(A.device).cuda_stream if stream is None else int(stream)
-        rc = gemm_run(self.handle, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
-                      _dtype_code(A), s)
+        if alpha == 1.0 and beta == 0.0 and out.dtype == torch.float32:
+            rc = gemm_run(self.handle, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
+                          _dtype_code(A), s)
+        else:
+            rc = gemm_run_ex(self.handle, M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb, float(beta),
+                             out.data_ptr(), ldc, _dtype_code(A), _dtype_code(out), s)
         if rc != GEMM_OK:
             raise GemmError(rc, "gemm_run")
         return out
@@ -257,7 +271,7 @@ class Gemm:
         return gemm_get_device_status(self.handle, s)
 
 
-__all__ = ["Gemm", "GemmError", "gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host",
+__all__ = ["Gemm", "GemmError", "gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host",
            "conv4d_im2col", "conv4d_forward", "gemm_get_device_status", "gemm_set_option", "gemm_launch_count",
            "gemm_status_string",
            "status_string", "library", "LIB_PATH", "EXPORTS"]

@@ -22,6 +22,8 @@ struct gemm_ctx {
     float* workspace = nullptr;
     size_t workspace_bytes = 0;
     void* stage[3] = {nullptr, nullptr, nullptr};  // gemm_run_host device copies of A, B, C
+    float* product = nullptr;  // fp32 product for the generalised epilogue of fp32 inputs
+    size_t product_bytes = 0;
     size_t stage_bytes[3] = {0, 0, 0};
     int opt_f32_kernel = 0;
     int opt_split_k = 0;
@@ -78,7 +80,7 @@ int ensure_buffer(void** buf, size_t* have, size_t bytes)
 }
 
 int check_common(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                 const void* B, int64_t ldb, const float* C, int64_t ldc, int dtype)
+                 const void* B, int64_t ldb, const void* C, int64_t ldc, int dtype)
 {
     if (!h) return GEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
@@ -175,6 +177,7 @@ int gemm_destroy(gemm_handle_t h)
     }
     if (h->d_status) cudaFree(h->d_status);
     if (h->workspace) cudaFree(h->workspace);
+    if (h->product) cudaFree(h->product);
     for (int i = 0; i < 3; ++i)
         if (h->stage[i]) cudaFree(h->stage[i]);
     delete h;
@@ -214,31 +217,62 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     }
 }
 
-int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-             const void* B, int64_t ldb, float* C, int64_t ldc, gemm_dtype_t dtype, void* stream)
+int gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                const void* B, int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t ab_dtype,
+                gemm_dtype_t c_dtype, void* stream)
 {
-    int rc = check_common(h, M, N, K, A, lda, B, ldb, C, ldc, (int)dtype);
-    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    int rc = check_common(h, M, N, K, A, lda, B, ldb, C, ldc, (int)ab_dtype);
+    if (rc != GEMM_OK) return rc;
+    if (c_dtype != GEMM_F32 && c_dtype != GEMM_BF16 && c_dtype != GEMM_F16) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    const size_t ces = (c_dtype == GEMM_F32) ? 4 : 2;
+    if (reinterpret_cast<uintptr_t>(C) & (ces - 1)) return GEMM_ERR_ALIGNMENT;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (dtype != GEMM_F32 && K > 0) {
+    if (ab_dtype != GEMM_F32 && K > 0) {
         // TMA tensor maps: 16-byte aligned bases, row strides a multiple of 16 bytes.
         if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) || (lda % 8) ||
             (ldb % 8))
             return GEMM_ERR_ALIGNMENT;
-        if ((reinterpret_cast<uintptr_t>(C) & 3)) return GEMM_ERR_ALIGNMENT;
     }
     DeviceGuard g(h->device);
     if (!g.ok()) return GEMM_ERR_CUDA;
-    if (K == 0) return from_cuda(cudaMemset2DAsync(C, (size_t)ldc * 4, 0, (size_t)N * 4, (size_t)M, s));
-    if (dtype == GEMM_F32) {
-        F32Args a{M, N, K, static_cast<const float*>(A), lda, static_cast<const float*>(B), ldb, C, ldc};
-        return run_f32(h, a, s);
+    Epilogue epi;
+    epi.alpha = alpha;
+    epi.beta = beta;
+    epi.c_dtype = (int)c_dtype;
+    if (K == 0) {  // empty product: C = beta * C
+        if (beta == 0.f) return from_cuda(cudaMemset2DAsync(C, (size_t)ldc * ces, 0, (size_t)N * ces, (size_t)M, s));
+        cudaError_t e = launch_epilogue(nullptr, 0, C, ldc, M, N, epi, h->num_sms, s);
+        if (e == cudaSuccess) h->launches += 1;
+        return from_cuda(e);
     }
-    TcArgs t{M, N, K, A, lda, B, ldb, C, ldc, dtype == GEMM_BF16 ? 1 : 0, h->opt_test_stall};
+    if (ab_dtype == GEMM_F32) {
+        if (epi.plain()) {
+            F32Args a{M, N, K, static_cast<const float*>(A), lda, static_cast<const float*>(B), ldb,
+                      static_cast<float*>(C), ldc};
+            return run_f32(h, a, s);
+        }
+        // fp32 product into a handle buffer, then the epilogue pass
+        rc = ensure_buffer(reinterpret_cast<void**>(&h->product), &h->product_bytes, (size_t)M * N * sizeof(float));
+        if (rc != GEMM_OK) return rc;
+        F32Args a{M, N, K, static_cast<const float*>(A), lda, static_cast<const float*>(B), ldb, h->product, N};
+        rc = run_f32(h, a, s);
+        if (rc != GEMM_OK) return rc;
+        cudaError_t e = launch_epilogue(h->product, N, C, ldc, M, N, epi, h->num_sms, s);
+        if (e == cudaSuccess) h->launches += 1;
+        return from_cuda(e);
+    }
+    TcArgs t{M, N, K, A, lda, B, ldb, C, ldc, ab_dtype == GEMM_BF16 ? 1 : 0, h->opt_test_stall, epi};
     int n = 0;
     int rc2 = launch_tc_gemm(t, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_tc_chunk, h->opt_tc_pair, s, &n);
     h->launches += n;
     return rc2;
+}
+
+int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+             int64_t ldb, float* C, int64_t ldc, gemm_dtype_t dtype, void* stream)
+{
+    return gemm_run_ex(h, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, dtype, GEMM_F32, stream);
 }
 
 }  // extern "C"

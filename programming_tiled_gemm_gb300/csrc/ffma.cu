@@ -17,6 +17,9 @@
 // shared buffers, one barrier per tile), M/N/K tails are predicated (zero fill), and an
 // optional split of K over grid.z with a fixed-order reduction fills the GPU when there
 // are few output tiles.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "internal.h"
 
 namespace gemm_gb300 {
@@ -421,6 +424,35 @@ splitk_reduce_kernel(const float* __restrict__ ws, int split, int64_t M, int64_t
     }
 }
 
+// C = alpha * P + beta * C (C unread when beta == 0), stored as fp32, bf16 or fp16.
+// P == nullptr stands for a zero product.
+template <int CT>
+__global__ void __launch_bounds__(256)
+epilogue_kernel(const float* __restrict__ P, int64_t ldp, void* C, int64_t ldc, int64_t M, int64_t N, float alpha,
+                float beta)
+{
+    const int64_t total = M * N;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        const int64_t m = idx / N, n = idx - m * N;
+        float v = P ? alpha * P[m * ldp + n] : 0.f;  // no P: an empty product (K == 0)
+        const int64_t c = m * ldc + n;
+        if (CT == GEMM_F32) {
+            float* out = static_cast<float*>(C);
+            if (beta != 0.f) v = fmaf(beta, out[c], v);
+            out[c] = v;
+        } else if (CT == GEMM_BF16) {
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(C);
+            if (beta != 0.f) v = fmaf(beta, __bfloat162float(out[c]), v);
+            out[c] = __float2bfloat16_rn(v);
+        } else {
+            __half* out = static_cast<__half*>(C);
+            if (beta != 0.f) v = fmaf(beta, __half2float(out[c]), v);
+            out[c] = __float2half_rn(v);
+        }
+    }
+}
+
 template <int BM, int BN, int BK, int TM, int TN>
 cudaError_t launch_variant(const F32Args& a, int split, float* ws, cudaStream_t stream, int* launches)
 {
@@ -522,6 +554,23 @@ cudaError_t launch_ffma_tiled(const F32Args& a, int variant, int split, float* w
     if (split < 1) split = 1;
     if (variant == 2) return launch_variant<64, 128, 16, 4, 8>(a, split, ws, stream, launches);
     return launch_warptile(a, split, ws, stream, launches);
+}
+
+cudaError_t launch_epilogue(const float* P, int64_t ldp, void* C, int64_t ldc, int64_t M, int64_t N,
+                            const Epilogue& epi, int num_sms, cudaStream_t stream)
+{
+    const int64_t total = M * N;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 152) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (epi.c_dtype == GEMM_BF16)
+        epilogue_kernel<GEMM_BF16><<<(unsigned)blocks, 256, 0, stream>>>(P, ldp, C, ldc, M, N, epi.alpha, epi.beta);
+    else if (epi.c_dtype == GEMM_F16)
+        epilogue_kernel<GEMM_F16><<<(unsigned)blocks, 256, 0, stream>>>(P, ldp, C, ldc, M, N, epi.alpha, epi.beta);
+    else
+        epilogue_kernel<GEMM_F32><<<(unsigned)blocks, 256, 0, stream>>>(P, ldp, C, ldc, M, N, epi.alpha, epi.beta);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t N, float* C,

@@ -17,6 +17,18 @@ enum DeviceStatus : int {
     kDevTimeoutDrain = 4      // a CTA gave up draining its own copies / MMAs before exit
 };
 
+// Output step of the generalised product: C = alpha * (A . B) + beta * C, C stored as
+// fp32, bf16 or fp16 (a gemm_dtype_t); C is not read when beta == 0.
+struct Epilogue {
+    float alpha = 1.f, beta = 0.f;
+    int c_dtype = 0;  // GEMM_F32, GEMM_BF16 or GEMM_F16
+    bool plain() const { return alpha == 1.f && beta == 0.f && c_dtype == 0; }
+};
+
+// C = alpha * P + beta * C over an M x N fp32 product P (row stride ldp).
+cudaError_t launch_epilogue(const float* P, int64_t ldp, void* C, int64_t ldc, int64_t M, int64_t N,
+                            const Epilogue& epi, int num_sms, cudaStream_t stream);
+
 struct F32Args {
     int64_t M, N, K;
     const float* A;
@@ -71,10 +83,11 @@ struct TcArgs {
     int64_t lda;
     const void* B;
     int64_t ldb;
-    float* C;
+    void* C;         // fp32, bf16 or fp16 per epi.c_dtype
     int64_t ldc;
     int is_bf16;     // 1 = bf16, 0 = fp16
     int test_stall;  // test hook: make a bounded wait run out (exercises the timeout path)
+    Epilogue epi;
 };
 // Returns GEMM_OK or a negative gemm_status_t.
 // kc_blocks: 64-wide k-blocks per accumulation chunk (0 = default 16).

@@ -38,6 +38,8 @@
 // returns; the host reads the code through gemm_get_device_status.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <mutex>
 
@@ -229,7 +231,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int m_blocks, int n_block
 
 struct TcParams {
     int M, N, K;
-    float* C;
+    void* C;  // fp32, bf16 or fp16 (c_dtype)
     int64_t ldc;
     int m_blocks, n_blocks, num_tiles, k_blocks;
     int kc;       // k-blocks per accumulation chunk
@@ -240,7 +242,75 @@ struct TcParams {
     int* status;
     uint64_t limit_ns;
     int test_stall;  // test hook: the epilogue first waits on a barrier nothing arrives on
+    float alpha, beta;  // C = alpha * (A . B) + beta * C; C unread when beta == 0
+    int c_dtype;        // GEMM_F32, GEMM_BF16 or GEMM_F16
+    int epi_plain;      // alpha == 1, beta == 0, fp32: plain stores
 };
+
+// Four adjacent outputs of the generalised product: C = alpha * acc + beta * C, in the
+// output type; one 16- or 8-byte access when `vec`, else element by element.
+__device__ __forceinline__ void epi_store4(const TcParams& p, int64_t off, int ncols, float a0, float a1, float a2,
+                                           float a3, bool vec)
+{
+    float v[4] = {p.alpha * a0, p.alpha * a1, p.alpha * a2, p.alpha * a3};
+    if (p.c_dtype == GEMM_F32) {
+        float* c = static_cast<float*>(p.C) + off;
+        if (vec) {
+            if (p.beta != 0.f) {
+                const float4 o = *reinterpret_cast<const float4*>(c);
+                v[0] = fmaf(p.beta, o.x, v[0]), v[1] = fmaf(p.beta, o.y, v[1]);
+                v[2] = fmaf(p.beta, o.z, v[2]), v[3] = fmaf(p.beta, o.w, v[3]);
+            }
+            *reinterpret_cast<float4*>(c) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < ncols) c[j] = (p.beta != 0.f) ? fmaf(p.beta, c[j], v[j]) : v[j];
+        }
+    } else if (p.c_dtype == GEMM_BF16) {
+        __nv_bfloat16* c = static_cast<__nv_bfloat16*>(p.C) + off;
+        if (vec) {
+            uint2 raw = make_uint2(0, 0);
+            if (p.beta != 0.f) raw = *reinterpret_cast<const uint2*>(c);
+            __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162*>(&raw.x), hi = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
+            if (p.beta != 0.f) {
+                v[0] = fmaf(p.beta, __low2float(lo), v[0]), v[1] = fmaf(p.beta, __high2float(lo), v[1]);
+                v[2] = fmaf(p.beta, __low2float(hi), v[2]), v[3] = fmaf(p.beta, __high2float(hi), v[3]);
+            }
+            lo = __floats2bfloat162_rn(v[0], v[1]);
+            hi = __floats2bfloat162_rn(v[2], v[3]);
+            raw.x = *reinterpret_cast<uint32_t*>(&lo);
+            raw.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(c) = raw;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < ncols)
+                    c[j] = __float2bfloat16_rn((p.beta != 0.f) ? fmaf(p.beta, __bfloat162float(c[j]), v[j]) : v[j]);
+        }
+    } else {
+        __half* c = static_cast<__half*>(p.C) + off;
+        if (vec) {
+            uint2 raw = make_uint2(0, 0);
+            if (p.beta != 0.f) raw = *reinterpret_cast<const uint2*>(c);
+            __half2 lo = *reinterpret_cast<__half2*>(&raw.x), hi = *reinterpret_cast<__half2*>(&raw.y);
+            if (p.beta != 0.f) {
+                v[0] = fmaf(p.beta, __low2float(lo), v[0]), v[1] = fmaf(p.beta, __high2float(lo), v[1]);
+                v[2] = fmaf(p.beta, __low2float(hi), v[2]), v[3] = fmaf(p.beta, __high2float(hi), v[3]);
+            }
+            lo = __floats2half2_rn(v[0], v[1]);
+            hi = __floats2half2_rn(v[2], v[3]);
+            raw.x = *reinterpret_cast<uint32_t*>(&lo);
+            raw.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(c) = raw;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < ncols)
+                    c[j] = __float2half_rn((p.beta != 0.f) ? fmaf(p.beta, __half2float(c[j]), v[j]) : v[j]);
+        }
+    }
+}
 
 __device__ __forceinline__ void record_error(int* status, int code, volatile int* abort_flag)
 {
@@ -440,8 +510,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!ok) break;
             const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
             const int row = tc.m_blk * BM + q * 32 + lane;
-            if (row < p.M) {
-                float* crow = p.C + (int64_t)row * p.ldc;
+            if (row < p.M && !p.epi_plain) {
+                const int col0 = tc.n_blk * BN + half * EPI_COLS;
+                const bool full = p.vec_store && col0 + EPI_COLS <= p.N;
+#pragma unroll
+                for (int j = 0; j < EPI_COLS; j += 4)
+                    if (col0 + j < p.N)
+                        epi_store4(p, (int64_t)row * p.ldc + col0 + j, p.N - (col0 + j), tot[j], tot[j + 1], tot[j + 2],
+                                   tot[j + 3], full);
+            } else if (row < p.M) {
+                float* crow = static_cast<float*>(p.C) + (int64_t)row * p.ldc;
                 const int col0 = tc.n_blk * BN + half * EPI_COLS;
                 if (p.vec_store && col0 + EPI_COLS <= p.N) {
 #pragma unroll
@@ -787,8 +865,16 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks, p.group_m);
             const int row = tc.m_blk * (2 * BM) + (int)rank * BM + q * 32 + lane;
-            if (row < p.M) {
-                float* crow = p.C + (int64_t)row * p.ldc;
+            if (row < p.M && !p.epi_plain) {
+                const int col0 = tc.n_blk * BN + half * EPI_COLS;
+                const bool full = p.vec_store && col0 + EPI_COLS <= p.N;
+#pragma unroll
+                for (int j = 0; j < EPI_COLS; j += 4)
+                    if (col0 + j < p.N)
+                        epi_store4(p, (int64_t)row * p.ldc + col0 + j, p.N - (col0 + j), tot[j], tot[j + 1], tot[j + 2],
+                                   tot[j + 3], full);
+            } else if (row < p.M) {
+                float* crow = static_cast<float*>(p.C) + (int64_t)row * p.ldc;
                 const int col0 = tc.n_blk * BN + half * EPI_COLS;
                 if (p.vec_store && col0 + EPI_COLS <= p.N) {
 #pragma unroll
@@ -882,7 +968,13 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.group_m = GROUP_M;
     p.nchunks = (p.k_blocks + p.kc - 1) / p.kc;
     p.idesc = make_idesc(bf16);
-    p.vec_store = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && (a.ldc % 4 == 0);
+    // vector stores: 4 outputs per access (16 bytes fp32, 8 bytes bf16/fp16)
+    const uintptr_t c_align = (a.epi.c_dtype == GEMM_F32) ? 15 : 7;
+    p.vec_store = ((reinterpret_cast<uintptr_t>(a.C) & c_align) == 0) && (a.ldc % 4 == 0);
+    p.alpha = a.epi.alpha;
+    p.beta = a.epi.beta;
+    p.c_dtype = a.epi.c_dtype;
+    p.epi_plain = a.epi.plain() ? 1 : 0;
     p.status = dev_status;
     p.limit_ns = wait_limit_ns;
     p.test_stall = a.test_stall;

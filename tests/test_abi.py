@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_header_declares_the_documented_entry_points():
     names = declared_functions()
-    for n in ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "conv4d_im2col", "conv4d_forward",
+    for n in ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host", "conv4d_im2col", "conv4d_forward",
               "gemm_get_device_status", "gemm_set_option", "gemm_launch_count", "gemm_status_string"]:
         assert n in names
 
@@ -59,6 +59,7 @@ def test_null_handle_is_rejected_without_touching_cuda(pkg):
     lib = pkg.library()
     assert lib.gemm_run(None, 4, 4, 4, 1, 4, 1, 4, 1, 4, 0, None) == pkg.GEMM_ERR_INVALID_ARG
     assert lib.gemm_run_host(None, 4, 4, 4, 1, 4, 1, 4, 1, 4, 0, None) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_run_ex(None, 4, 4, 4, 1.0, 1, 4, 1, 4, 0.0, 1, 4, 0, 0, None) == pkg.GEMM_ERR_INVALID_ARG
     assert lib.gemm_set_option(None, 1, 0) == pkg.GEMM_ERR_INVALID_ARG
     assert lib.gemm_get_device_status(None, None) == pkg.GEMM_ERR_INVALID_ARG
     assert lib.gemm_destroy(None) == pkg.GEMM_OK
