@@ -111,8 +111,12 @@ int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)
                 : (kernel == 3) ? skinny_auto_split(a, h->num_sms)
                                 : ffma_auto_split(a, kernel, h->num_sms);
     if ((int64_t)split > a.K) split = (int)(a.K > 0 ? a.K : 1);
-    if (split > 1) {
-        const size_t need = (size_t)split * (size_t)a.M * (size_t)a.N * sizeof(float);
+    size_t need = (split > 1) ? (size_t)split * (size_t)a.M * (size_t)a.N * sizeof(float) : 0;
+    if (kernel == 1) {
+        const size_t rem = (size_t)ffma_remainder_workspace(a, kernel, split, h->num_sms) * sizeof(float);
+        if (rem > need) need = rem;
+    }
+    if (need > 0) {
         int rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, need);
         if (rc != GEMM_OK) return rc;
     }

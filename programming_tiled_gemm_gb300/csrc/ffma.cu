@@ -226,10 +226,38 @@ constexpr int W_BM = 128, W_BN = 128, W_BK = 16;
 // GB300 (54.7 TFLOP/s at 4096^3) than two blocks capped at 128 registers (49.8, spilling).
 int g_warptile_min_blocks = 1;
 
+// A last, partial wave of interior tiles leaves SMs idle for a whole tile time.  Its tiles
+// can instead run cut along K into `rs` pieces (K slices of one tile, summed in fixed order
+// afterwards): the remainder then takes ceil(rem * rs / slots) / rs tile times.  Returns the
+// remainder tile count and the split (rs = 1, rem = 0 when it does not pay).
+void remainder_plan(int64_t interior, int64_t slots, int64_t K, int* rem_out, int* rs_out)
+{
+    *rem_out = 0;
+    *rs_out = 1;
+    if (slots <= 0 || interior <= slots) return;
+    const int64_t rem = interior % slots;
+    if (rem == 0) return;
+    double best_t = 1.0;
+    int best_rs = 1;
+    for (int rs = 2; rs <= 8; ++rs) {
+        if (K / rs < 32 * W_BK) break;  // keep at least 32 k-tiles per piece
+        const double t = (double)((rem * rs + slots - 1) / slots) / rs;
+        if (t < best_t - 1e-9) {
+            best_t = t;
+            best_rs = rs;
+        }
+    }
+    if (best_t > 0.85) return;
+    *rem_out = (int)rem;
+    *rs_out = best_rs;
+}
+
 struct TileMap {
     int mode;        // 0: grouped raster over rows x cols tiles; 1: L-shaped edge region
     int rows, cols;  // mode 0: tile grid; mode 1: full tile rows / cols (interior extent)
     int m_tiles, n_tiles;
+    int first = 0;    // index of the block's tile = first + blockIdx.x
+    int compact = 0;  // split-K partials go to a per-tile workspace [split][blocks][BM*BN]
 };
 
 __device__ __forceinline__ void map_tile(const TileMap& t, int pid, int& mt, int& nt)
@@ -264,14 +292,21 @@ ffma_warptile_kernel(F32Args p, int64_t k_per_split, TileMap tmap, float* ws, in
 
     const int tid = threadIdx.x;
     int mt, nt;
-    map_tile(tmap, blockIdx.x, mt, nt);
+    map_tile(tmap, tmap.first + blockIdx.x, mt, nt);
     const int64_t m0 = (int64_t)mt * W_BM, n0 = (int64_t)nt * W_BN;
     const int64_t kbeg = (int64_t)blockIdx.z * k_per_split;
     const int64_t kend = min(p.K, kbeg + k_per_split);
 
+    // output rows: C, or a split-K partial (a full M x N slice, or one BM x BN tile);
+    // element (gm, gn) lives at out[(gm - row0) * ldo + (gn - col0)]
     float* out;
-    int64_t ldo;
-    if (gridDim.z > 1) {
+    int64_t ldo, row0 = 0, col0 = 0;
+    if (tmap.compact) {
+        out = ws + ((int64_t)blockIdx.z * gridDim.x + blockIdx.x) * (W_BM * W_BN);
+        ldo = W_BN;
+        row0 = m0;
+        col0 = n0;
+    } else if (gridDim.z > 1) {
         out = ws + (int64_t)blockIdx.z * p.M * p.N;
         ldo = p.N;
     } else {
@@ -393,12 +428,12 @@ ffma_warptile_kernel(F32Args p, int64_t k_per_split, TileMap tmap, float* ws, in
     for (int i = 0; i < 8; ++i) {
         const int64_t gm = m0 + a_frag + (i / 4) * 32 + (i % 4);
         if (EDGE && gm >= p.M) continue;
-        float* row = out + gm * ldo;
+        float* row = out + (gm - row0) * ldo - col0;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int64_t gn = n0 + b_frag + h * 16;
             const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y};
-            if (vec_out && (!EDGE || gn + 3 < p.N)) {
+            if ((vec_out || tmap.compact) && (!EDGE || gn + 3 < p.N)) {
                 *reinterpret_cast<float4*>(row + gn) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
@@ -406,6 +441,31 @@ ffma_warptile_kernel(F32Args p, int64_t k_per_split, TileMap tmap, float* ws, in
                     if (gn + j < p.N) row[gn + j] = v[j];
             }
         }
+    }
+}
+
+// Fixed-order sum of per-tile split-K partials (compact layout [split][tiles][BM*BN]):
+// C[tile element] = part 0 + part 1 + ... for the tiles first .. first + ntiles - 1.
+__global__ void __launch_bounds__(256)
+splitk_reduce_tiles_kernel(const float* __restrict__ ws, int split, TileMap tmap, int ntiles, float* __restrict__ C,
+                           int64_t ldc)
+{
+    constexpr int TILE = W_BM * W_BN;
+    const int64_t total = (int64_t)ntiles * TILE / 4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += stride) {
+        const int64_t e = q * 4;
+        const int t = (int)(e / TILE);
+        const int w = (int)(e % TILE);
+        float4 s = *reinterpret_cast<const float4*>(ws + e);
+        for (int z = 1; z < split; ++z) {
+            const float4 v = *reinterpret_cast<const float4*>(ws + (int64_t)z * ntiles * TILE + e);
+            s.x += v.x, s.y += v.y, s.z += v.z, s.w += v.w;
+        }
+        int mt, nt;
+        map_tile(tmap, tmap.first + t, mt, nt);
+        float* dst = C + ((int64_t)mt * W_BM + w / W_BN) * ldc + (int64_t)nt * W_BN + w % W_BN;
+        dst[0] = s.x, dst[1] = s.y, dst[2] = s.z, dst[3] = s.w;
     }
 }
 
@@ -485,7 +545,7 @@ cudaError_t launch_variant(const F32Args& a, int split, float* ws, cudaStream_t 
 
 template <int MIN_BLOCKS>
 cudaError_t launch_warptile_occ(const F32Args& a, int64_t kps, int nsplit, float* ws, int vec_in, int vec_out,
-                                cudaStream_t stream, int* launches)
+                                int64_t remainder_slots, cudaStream_t stream, int* launches)
 {
     const int m_tiles = (int)((a.M + W_BM - 1) / W_BM), n_tiles = (int)((a.N + W_BN - 1) / W_BN);
     const int m_full = (int)(a.M / W_BM), n_full = (int)(a.N / W_BN);
@@ -493,12 +553,37 @@ cudaError_t launch_warptile_occ(const F32Args& a, int64_t kps, int nsplit, float
     const int interior = fast_ok ? m_full * n_full : 0;
     const int64_t edge = (int64_t)m_tiles * n_tiles - interior;
     if (interior > 0) {
+        // whole waves as usual; the tiles of a last, partial wave (if any) are cut along
+        // K so that they fill the GPU's `remainder_slots` block slots (remainder_plan)
+        int rem = 0, rs = 1;
+        if (remainder_slots > 0) remainder_plan(interior, remainder_slots, a.K, &rem, &rs);
+        const int main_tiles = interior - rem;
         TileMap t{0, m_full, n_full, m_tiles, n_tiles};
-        ffma_warptile_kernel<MIN_BLOCKS, false><<<dim3(interior, 1, nsplit), kThreads, 0, stream>>>(
-            a, kps, t, ws, vec_in, vec_out);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        *launches += 1;
+        if (main_tiles > 0) {
+            ffma_warptile_kernel<MIN_BLOCKS, false><<<dim3(main_tiles, 1, nsplit), kThreads, 0, stream>>>(
+                a, kps, t, ws, vec_in, vec_out);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            *launches += 1;
+        }
+        if (rem > 0) {
+            int64_t rkps = (a.K + rs - 1) / rs;
+            rkps = (rkps + W_BK - 1) / W_BK * W_BK;
+            const int rsplit = (int)((a.K + rkps - 1) / rkps);
+            TileMap tr = t;
+            tr.first = main_tiles;
+            tr.compact = 1;
+            ffma_warptile_kernel<MIN_BLOCKS, false><<<dim3(rem, 1, rsplit), kThreads, 0, stream>>>(
+                a, rkps, tr, ws, vec_in, vec_out);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            int64_t blocks = (int64_t)rem * W_BM * W_BN / 4 / 256;
+            if (blocks < 1) blocks = 1;
+            splitk_reduce_tiles_kernel<<<(unsigned)blocks, 256, 0, stream>>>(ws, rsplit, tr, rem, a.C, a.ldc);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            *launches += 2;
+        }
     }
     if (edge > 0) {
         TileMap t = fast_ok ? TileMap{1, m_full, n_full, m_tiles, n_tiles} : TileMap{0, m_tiles, n_tiles, m_tiles, n_tiles};
@@ -511,7 +596,8 @@ cudaError_t launch_warptile_occ(const F32Args& a, int64_t kps, int nsplit, float
     return cudaSuccess;
 }
 
-cudaError_t launch_warptile(const F32Args& a, int split, float* ws, cudaStream_t stream, int* launches)
+cudaError_t launch_warptile(const F32Args& a, int split, float* ws, int remainder_split, int num_sms,
+                            cudaStream_t stream, int* launches)
 {
     const int64_t m_tiles = (a.M + W_BM - 1) / W_BM, n_tiles = (a.N + W_BN - 1) / W_BN;
     if (m_tiles * n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -525,15 +611,28 @@ cudaError_t launch_warptile(const F32Args& a, int split, float* ws, cudaStream_t
         vec_out = (a.N % 4 == 0);
     else
         vec_out = (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0;
+    const int64_t slots = (nsplit == 1 && remainder_split) ? (int64_t)num_sms * g_warptile_min_blocks : 0;
     cudaError_t e = (g_warptile_min_blocks == 1)
-                        ? launch_warptile_occ<1>(a, kps, nsplit, ws, vec_in, vec_out, stream, launches)
-                        : launch_warptile_occ<2>(a, kps, nsplit, ws, vec_in, vec_out, stream, launches);
+                        ? launch_warptile_occ<1>(a, kps, nsplit, ws, vec_in, vec_out, slots, stream, launches)
+                        : launch_warptile_occ<2>(a, kps, nsplit, ws, vec_in, vec_out, slots, stream, launches);
     if (e != cudaSuccess || nsplit == 1) return e;
     *launches += 1;
     return launch_splitk_reduce(ws, nsplit, a.M, a.N, a.C, a.ldc, 0, stream);
 }
 
 }  // namespace
+
+int64_t ffma_remainder_workspace(const F32Args& a, int variant, int split, int num_sms)
+{
+    // floats of workspace the remainder-wave split needs (0 when it does not apply)
+    if (variant == 2 || split > 1) return 0;
+    const bool vec_in = ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15) == 0 &&
+                        a.lda % 4 == 0 && a.ldb % 4 == 0;
+    if (!vec_in || a.K % W_BK) return 0;
+    int rem = 0, rs = 1;
+    remainder_plan((a.M / W_BM) * (a.N / W_BN), (int64_t)num_sms * g_warptile_min_blocks, a.K, &rem, &rs);
+    return (int64_t)rem * rs * W_BM * W_BN;
+}
 
 int ffma_auto_split(const F32Args& a, int variant, int num_sms)
 {
@@ -550,10 +649,9 @@ int ffma_auto_split(const F32Args& a, int variant, int num_sms)
 cudaError_t launch_ffma_tiled(const F32Args& a, int variant, int split, float* ws, int num_sms,
                               cudaStream_t stream, int* launches)
 {
-    (void)num_sms;
     if (split < 1) split = 1;
     if (variant == 2) return launch_variant<64, 128, 16, 4, 8>(a, split, ws, stream, launches);
-    return launch_warptile(a, split, ws, stream, launches);
+    return launch_warptile(a, split, ws, 1, num_sms, stream, launches);
 }
 
 cudaError_t launch_epilogue(const float* P, int64_t ldp, void* C, int64_t ldc, int64_t M, int64_t N,

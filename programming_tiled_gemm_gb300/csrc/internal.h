@@ -61,6 +61,10 @@ cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t 
 
 // Every launcher adds the number of kernels it launched to *launches.
 
+// Workspace floats the 128x128 FFMA path needs to split the tiles of a last, partial wave
+// along K (0 when it does not apply).
+int64_t ffma_remainder_workspace(const F32Args& a, int variant, int split, int num_sms);
+
 // Split factors the launchers would pick on their own (0 in the option = auto).
 int ffma_auto_split(const F32Args& a, int variant, int num_sms);
 int skinny_auto_split(const F32Args& a, int num_sms);

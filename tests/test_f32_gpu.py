@@ -154,6 +154,39 @@ def test_config_skinny_full_matrix(lib):
     assert np.array_equal(C, ref_of(Ai, Bi))
 
 
+def last_wave_plan(interior, slots, K):
+    """The launcher's rule for the tiles of a last, partial wave: (tiles, pieces along K)."""
+    if interior <= slots or interior % slots == 0:
+        return 0, 1
+    rem = interior % slots
+    best_t, best_rs = 1.0, 1
+    for rs in range(2, 9):
+        if K // rs < 32 * 16:
+            break
+        t = ((rem * rs + slots - 1) // slots) / rs
+        if t < best_t - 1e-9:
+            best_t, best_rs = t, rs
+    return (0, 1) if best_t > 0.85 else (rem, best_rs)
+
+
+@pytest.mark.parametrize("M,N", [(1664, 1664), (1701, 1669)])
+def test_last_wave_tiles_split_along_K(lib, M, N):
+    # 13 x 13 = 169 interior 128 x 128 tiles: on 152 SMs the 17 tiles of the last wave run
+    # cut into K slices whose partial tiles are summed in a separate fixed-order pass
+    K = 2048
+    slots = torch.cuda.get_device_properties(0).multi_processor_count
+    rem, rs = last_wave_plan((M // 128) * (N // 128), slots, K)
+    Ai, Bi = si.integer_copy(M, N, K, seed=M)
+    n0 = lib.launch_count()
+    got = run_padded(lib, Ai, Bi, pad_b=-N % 4, pad_c=4)  # rows of B 16-byte aligned: vector loads
+    edge = (M % 128 != 0) or (N % 128 != 0)
+    assert lib.launch_count() - n0 == 1 + (2 if rem else 0) + (1 if edge else 0)
+    assert np.array_equal(got, ref_of(Ai, Bi))
+    A, B = si.gemm_operands(M, N, K, seed=M + 1)
+    got = run_padded(lib, A, B)
+    assert np.abs(got - ref_of(A, B)).max() <= 1e-5 * math.sqrt(K)
+
+
 def test_results_are_deterministic(lib):
     import programming_tiled_gemm_gb300 as g
     A, B = si.gemm_operands(24, 3000, 5000, seed=9)
