@@ -144,6 +144,25 @@ int conv4d_im2col(gemm_handle_t h, const float* x, int64_t C_in, const int64_t i
 int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4], const float* w,
                    int64_t C_out, const int64_t k_dims[4], float* y, int64_t ldy, void* stream);
 
+/* The same valid 4-D cross-correlation on the tensor cores, with 16-bit channel-last
+ * operands ("Three X: large convolutions in PyTorch for training", section "CUTLASS":
+ * the tensor-core implicit GEMM wants 128-bit aligned tensors, channel counts that are
+ * multiples of the MMA's K and channel-last memory order).
+ *   x : [in[0]][in[1]][in[2]][in[3]][C_in], bf16 or fp16 (`dtype`), contiguous, device.
+ *   w : [C_out][k[0]][k[1]][k[2]][k[3]][C_in], the same type, contiguous, device.
+ *   y : fp32 [P0][P1][P2][P3][C_out], contiguous, device, Pd = in[d] - k[d] + 1;
+ *       overwritten.  y[p][o] = sum over taps r and channels c of x[p + r][c] * w[o][r][c].
+ * Products of 16-bit values are exact in fp32; the tensor core accumulates in fp32, with
+ * consecutive 16-channel steps of the taps going round-robin to up to 8 partial sums
+ * (8 for C_out = 32, 512 / (2 C_out) in general) that are added in fp32
+ * round-to-nearest, in order.  Deterministic.  Asynchronous on `stream`; allocates
+ * nothing.  x, w and y must be 16-byte aligned (GEMM_ERR_ALIGNMENT).
+ * GEMM_ERR_INVALID_ARG for bad extents, pointers or dtype (GEMM_BF16 or GEMM_F16 only);
+ * GEMM_ERR_UNSUPPORTED unless C_in % 16 == 0, C_out % 16 == 0, C_out <= 256,
+ * in[3] <= 256, and the staged input rows of one filter row fit in shared memory. */
+int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
+                      int64_t C_out, const int64_t k_dims[4], float* y, int dtype, void* stream);
+
 /* Synchronise `stream`, then read and clear the handle's device status word.
  * Returns GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a kernel launched through this
  * handle gave up on a bounded wait since the last call (its output is then invalid),
@@ -164,7 +183,7 @@ typedef enum {
     GEMM_OPT_TC_PAIR = 5,       /* tensor-core tiles: 0 choose (default: pairs when M > 128), 1 one CTA per
                                    128x256 tile, 2 a pair of CTAs (cluster of two) per 256x256 tile */
     GEMM_OPT_TEST_STALL = 6     /* test hook for failure detection, 0 (default) or 1: the kernels with
-                                   bounded waits (tensor-core GEMMs, TMA skinny GEMM) first wait on a
+                                   bounded waits (tensor-core GEMMs and convolution, TMA skinny GEMM) first wait on a
                                    barrier nothing arrives on; the wait runs out after the wait limit, the
                                    kernel drains its copies and MMAs, frees its tensor memory, returns,
                                    and gemm_get_device_status reports GEMM_ERR_DEVICE_TIMEOUT.  C is not

@@ -25,7 +25,7 @@ GEMM_OPT_TEST_STALL = 6
 
 # Every symbol include/gemm.h declares (the ABI test checks the library exports them).
 EXPORTS = ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host", "conv4d_im2col",
-           "conv4d_forward",
+           "conv4d_forward", "conv4d_forward_cl",
            "gemm_get_device_status", "gemm_set_option", "gemm_launch_count", "gemm_status_string",
            "gemm_run_f32_skinny_noalloc"]
 
@@ -49,6 +49,7 @@ def _load():
     lib.gemm_run_ex.argtypes = [p, i64, i64, i64, f32, p, i64, p, i64, f32, p, i64, i32, i32, p]
     lib.conv4d_im2col.argtypes = [p, p, i64, ctypes.POINTER(i64), ctypes.POINTER(i64), p, p]
     lib.conv4d_forward.argtypes = [p, p, i64, ctypes.POINTER(i64), p, i64, ctypes.POINTER(i64), p, i64, p]
+    lib.conv4d_forward_cl.argtypes = [p, p, i64, ctypes.POINTER(i64), p, i64, ctypes.POINTER(i64), p, i32, p]
     lib.gemm_get_device_status.argtypes = [p, p]
     lib.gemm_set_option.argtypes = [p, i32, i64]
     lib.gemm_launch_count.argtypes = [p]
@@ -106,6 +107,12 @@ def conv4d_forward(h, x, C_in, in_dims, w, C_out, k_dims, y, ldy, stream=0) -> i
     ins = (ctypes.c_int64 * 4)(*[int(v) for v in in_dims])
     ks = (ctypes.c_int64 * 4)(*[int(v) for v in k_dims])
     return _lib.conv4d_forward(h, x, C_in, ins, w, C_out, ks, y, ldy, stream)
+
+
+def conv4d_forward_cl(h, x, C_in, in_dims, w, C_out, k_dims, y, dtype, stream=0) -> int:
+    ins = (ctypes.c_int64 * 4)(*[int(v) for v in in_dims])
+    ks = (ctypes.c_int64 * 4)(*[int(v) for v in k_dims])
+    return _lib.conv4d_forward_cl(h, x, C_in, ins, w, C_out, ks, y, dtype, stream)
 
 
 def gemm_get_device_status(h, stream=0) -> int:
@@ -253,6 +260,30 @@ class Gemm:
             raise GemmError(rc, "conv4d_forward")
         return out.view(cout, *outs) if out.is_contiguous() else out
 
+    def conv4d_cl(self, x, w, out=None, stream=None):
+        """Valid 4-D cross-correlation on the tensor cores, channel-last 16-bit operands.
+
+        x: [I0, I1, I2, I3, C_in] and w: [C_out, R0, R1, R2, R3, C_in], both bf16 or both
+        fp16, contiguous; returns y: fp32 [P0, P1, P2, P3, C_out]."""
+        import torch
+        dt = {torch.bfloat16: GEMM_BF16, torch.float16: GEMM_F16}.get(x.dtype)
+        if x.dim() != 5 or w.dim() != 6 or dt is None or w.dtype != x.dtype:
+            raise ValueError("x must be [I0..I3, C_in] and w [C_out, R0..R3, C_in], both bf16 or both fp16")
+        if not (x.is_contiguous() and w.is_contiguous()) or w.shape[5] != x.shape[4]:
+            raise ValueError("x and w must be contiguous with the same C_in")
+        cin, cout = x.shape[4], w.shape[0]
+        ins, ks = list(x.shape[:4]), list(w.shape[1:5])
+        outs = [i - k + 1 for i, k in zip(ins, ks)]
+        if out is None:
+            out = torch.empty(outs + [cout], dtype=torch.float32, device=x.device)
+        elif list(out.shape) != outs + [cout] or out.dtype != torch.float32 or not out.is_contiguous():
+            raise ValueError("out must be contiguous fp32 %s" % (outs + [cout],))
+        s = torch.cuda.current_stream(x.device).cuda_stream if stream is None else int(stream)
+        rc = conv4d_forward_cl(self.handle, x.data_ptr(), cin, ins, w.data_ptr(), cout, ks, out.data_ptr(), dt, s)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "conv4d_forward_cl")
+        return out
+
     def conv4d(self, x, w, col=None, out=None, stream=None):
         """Valid 4-D cross-correlation as im2col + GEMM: y[C_out, P0, P1, P2, P3]."""
         ks = list(w.shape[2:])
@@ -272,6 +303,6 @@ class Gemm:
 
 
 __all__ = ["Gemm", "GemmError", "gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host",
-           "conv4d_im2col", "conv4d_forward", "gemm_get_device_status", "gemm_set_option", "gemm_launch_count",
+           "conv4d_im2col", "conv4d_forward", "conv4d_forward_cl", "gemm_get_device_status", "gemm_set_option", "gemm_launch_count",
            "gemm_status_string",
            "status_string", "library", "LIB_PATH", "EXPORTS"]

@@ -435,6 +435,26 @@ int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t 
     return GEMM_OK;
 }
 
+int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
+                      int64_t C_out, const int64_t k_dims[4], float* y, int dtype, void* stream)
+{
+    if (!h || !x || !w || !y || !in_dims || !k_dims || C_in <= 0 || C_out <= 0) return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_BF16 && dtype != GEMM_F16) return GEMM_ERR_INVALID_ARG;
+    for (int d = 0; d < 4; ++d)
+        if (in_dims[d] <= 0 || k_dims[d] <= 0 || k_dims[d] > in_dims[d] || in_dims[d] > (1 << 20))
+            return GEMM_ERR_INVALID_ARG;
+    if (C_in > (1 << 20) || C_out > (1 << 20)) return GEMM_ERR_INVALID_ARG;
+    if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(y)) & 15) != 0)
+        return GEMM_ERR_ALIGNMENT;
+    DeviceGuard g(h->device);
+    if (!g.ok()) return GEMM_ERR_CUDA;
+    int n = 0;
+    const int rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, dtype == GEMM_BF16, h->d_status,
+                                    h->wait_limit_ns, h->opt_test_stall, reinterpret_cast<cudaStream_t>(stream), &n);
+    h->launches += n;
+    return rc;
+}
+
 int gemm_get_device_status(gemm_handle_t h, void* stream)
 {
     if (!h) return GEMM_ERR_INVALID_ARG;

@@ -1,6 +1,8 @@
 // Internal declarations shared by the library's translation units (not installed).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -61,6 +63,9 @@ cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t 
 
 // Every launcher adds the number of kernels it launched to *launches.
 
+// The driver's cuTensorMapEncodeTiled (looked up once), or nullptr if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 // Workspace floats the 128x128 FFMA path needs to split the tiles of a last, partial wave
 // along K (0 when it does not apply).
 int64_t ffma_remainder_workspace(const F32Args& a, int variant, int split, int num_sms);
@@ -72,6 +77,12 @@ int skinny_auto_split(const F32Args& a, int num_sms);
 // 4-D valid cross-correlation lowering (im2col).
 cudaError_t launch_im2col4d(const float* x, int64_t cin, const int64_t in[4], const int64_t k[4],
                             float* col, int num_sms, cudaStream_t stream);
+
+// Valid 4-D cross-correlation on the tensor cores, channel-last 16-bit operands
+// (conv4d_forward_cl).  Returns a gemm_status_t.
+int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void* w, int64_t cout,
+                     const int64_t k[4], float* y, bool bf16, int* dev_status, uint64_t limit_ns, int test_stall,
+                     cudaStream_t stream, int* launches);
 
 // Valid 4-D cross-correlation as an implicit GEMM (no column matrix), C_out <= 32 per
 // launch.  y[o][p] at y + o*ldy + p; split > 1 uses `workspace` ([split][cout][npos]).

@@ -20,9 +20,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <mutex>
 
 #include "internal.h"
+#include "ptx.h"
 
 namespace gemm_gb300 {
 namespace {
@@ -38,7 +38,6 @@ constexpr int ST_STAGES = 6;
 template <int MR, int COLW, int MSPLIT>
 struct StCfg {
     static constexpr int COLS = 4 * 32 * COLW;                    // columns per work item
-    static constexpr int BOXES = COLS / ST_BOX_COLS;
     static constexpr int CONSUMER_WARPS = COLW * MSPLIT;
     static constexpr int THREADS = 32 * (1 + CONSUMER_WARPS);
     static constexpr int RT = MR / MSPLIT;                        // rows per consumer thread
@@ -47,60 +46,6 @@ struct StCfg {
     static constexpr int BYTES = ST_STAGES * (B_STAGE_BYTES + A_STAGE_BYTES) + 256 + 1024;
     static_assert(COLS % ST_BOX_COLS == 0 && MR % MSPLIT == 0 && RT % 2 == 0, "shape");
 };
-
-__device__ __forceinline__ uint32_t st_smem_u32(const void* p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t st_timer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void st_mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void st_mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-// Raise the phase's expected transaction bytes without arriving.
-__device__ __forceinline__ void st_mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool st_mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.b32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-// Bounded wait; gives up at the wall-clock limit or once another thread has aborted.
-__device__ __forceinline__ bool st_mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                             volatile int* abort_flag)
-{
-    if (st_mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = st_timer();
-    while (true) {
-        if (st_mbar_try_wait(bar, parity)) return true;
-        if ((abort_flag && *abort_flag) || st_timer() - t0 > limit_ns) return false;
-    }
-}
-__device__ __forceinline__ void st_tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
 
 struct StParams {
     F32Args a;
@@ -125,7 +70,7 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
     constexpr int ST_COLS = SM::COLS;
     constexpr int ST_B_STAGE_BYTES = SM::B_STAGE_BYTES;
     extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = st_smem_u32(smem_raw);
+    const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
     uint8_t* smem_b = smem;                                      // [ST_STAGES][ST_KROWS][ST_COLS] fp32
     float2* smem_a = reinterpret_cast<float2*>(smem + ST_STAGES * ST_B_STAGE_BYTES);  // [ST_STAGES][ST_KROWS][MR]
@@ -141,10 +86,10 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST_STAGES; ++s) {
-            st_mbar_init(st_smem_u32(&full_bar[s]), 1);
-            st_mbar_init(st_smem_u32(&empty_bar[s]), CONSUMER_WARPS);
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), CONSUMER_WARPS);
         }
-        st_mbar_init(st_smem_u32(never_bar), 1);
+        mbar_init(smem_u32(never_bar), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
@@ -173,7 +118,7 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
                     const int64_t gk = k0 + kk;
                     av[i] = (m < a.M && gk < kend) ? __ldg(a.A + (int64_t)m * a.lda + gk) : 0.f;
                 }
-                bool got = (lane == 0) ? st_mbar_wait(st_smem_u32(&empty_bar[stage]), phase ^ 1, p.limit_ns, abort_flag)
+                bool got = (lane == 0) ? mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.limit_ns, abort_flag)
                                        : true;
                 got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
                 if (!got) {
@@ -184,13 +129,13 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
                     ok = false;
                     break;
                 }
-                const uint32_t fb = st_smem_u32(&full_bar[stage]);
+                const uint32_t fb = smem_u32(&full_bar[stage]);
                 if (lane == 0) {
-                    st_mbar_expect_tx(fb, ST_B_STAGE_BYTES);
+                    mbar_expect_tx(fb, ST_B_STAGE_BYTES);
                     uint8_t* dst = smem_b + stage * ST_B_STAGE_BYTES;
 #pragma unroll
                     for (int j = 0; j < ST_COLS / ST_BOX_COLS; ++j)
-                        st_tma_load_2d(st_smem_u32(dst + j * ST_BOX_COLS * 4 * ST_KROWS), &tmB, fb, col0 + j * ST_BOX_COLS,
+                        tma_load_2d(smem_u32(dst + j * ST_BOX_COLS * 4 * ST_KROWS), &tmB, fb, col0 + j * ST_BOX_COLS,
                                        (int)k0);
                     issued_mask |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -205,7 +150,7 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
                 __syncwarp();
                 // the A writes of all lanes are ordered before this arrival (syncwarp);
                 // the barrier completes once the B bytes have landed too
-                if (lane == 0) st_mbar_arrive(fb);
+                if (lane == 0) mbar_arrive(fb);
                 if (++stage == ST_STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -216,7 +161,7 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
         if (lane == 0)
             for (int s = 0; s < ST_STAGES; ++s)
                 if ((issued_mask >> s) & 1)
-                    if (!st_mbar_wait(st_smem_u32(&full_bar[s]), (last_parity >> s) & 1, p.limit_ns, nullptr))
+                    if (!mbar_wait(smem_u32(&full_bar[s]), (last_parity >> s) & 1, p.limit_ns, nullptr))
                         atomicCAS(p.status, 0, kDevTimeoutDrain);
     } else {
         // ------------------------------------------------------------ consumer warps
@@ -228,7 +173,7 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
         int item_first = blockIdx.x;
         if (p.test_stall) {
             // test hook: a wait nothing will satisfy runs out and takes the abort path
-            bool got = st_mbar_wait(st_smem_u32(never_bar), 0, p.limit_ns, abort_flag);
+            bool got = mbar_wait(smem_u32(never_bar), 0, p.limit_ns, abort_flag);
             got = __all_sync(0xffffffffu, got);
             if (!got && lane == 0) {
                 atomicCAS(p.status, 0, kDevTimeoutMma);
@@ -248,7 +193,7 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
             for (int m = 0; m < RT; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
             bool ok = true;
             for (int64_t k0 = kbeg; k0 < kend; k0 += ST_KROWS) {
-                bool got = st_mbar_wait(st_smem_u32(&full_bar[stage]), phase, p.limit_ns, abort_flag);
+                bool got = mbar_wait(smem_u32(&full_bar[stage]), phase, p.limit_ns, abort_flag);
                 got = __all_sync(0xffffffffu, got);
                 if (!got) {
                     if (lane == 0) {
@@ -276,7 +221,7 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) st_mbar_arrive(st_smem_u32(&empty_bar[stage]));
+                if (lane == 0) mbar_arrive(smem_u32(&empty_bar[stage]));
                 if (++stage == ST_STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -314,28 +259,13 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
     __syncthreads();
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 st_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
 template <int MR, int COLW, int MSPLIT>
 cudaError_t launch_mr_tma(const F32Args& a, int split, float* ws, int num_sms, int* dev_status,
                           uint64_t limit_ns, int test_stall, cudaStream_t stream, int* launches)
 {
     // B as a [K][N] fp32 tensor, box 256 columns x 8 rows, no swizzle, zero fill outside
     CUtensorMap tmB;
-    auto enc = st_encoder();
+    auto enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.K};
     cuuint64_t strides[1] = {(cuuint64_t)a.ldb * 4};

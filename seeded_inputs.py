@@ -105,6 +105,14 @@ def workload_operands(w: Workload):
     return x, wt
 
 
+def channel_last(x: torch.Tensor, wt: torch.Tensor, dtype: str = "bf16"):
+    """The convolution's operands in channel-last order, rounded to a 16-bit dtype:
+    x [C_in, I0..I3] -> [I0..I3, C_in] and w [C_out, C_in, R0..R3] -> [C_out, R0..R3, C_in]
+    (a copy of the same values; nothing else changes)."""
+    return (_cast(x.permute(1, 2, 3, 4, 0).contiguous(), dtype),
+            _cast(wt.permute(0, 2, 3, 4, 5, 1).contiguous(), dtype))
+
+
 def sample_indices(M: int, N: int, seed: int, n_rows: int = 128, n_cols: int = 128, n_rand: int = 65536):
     """Deterministic sample of output positions: full rows, full columns, random entries."""
     g = generator(seed)
