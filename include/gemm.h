@@ -181,7 +181,8 @@ typedef enum {
                                    (1..4096): the tensor core's fp32 accumulator is restarted every chunk and
                                    chunk sums are added in fp32 round-to-nearest */
     GEMM_OPT_TC_PAIR = 5,       /* tensor-core tiles: 0 choose (default: pairs when M > 128), 1 one CTA per
-                                   128x256 tile, 2 a pair of CTAs (cluster of two) per 256x256 tile */
+                                   128x256 tile, 2 a pair of CTAs (cluster of two) per 256x256 tile, 3 two
+                                   pairs (cluster of four) per 512x256 tile, B read once for both pairs */
     GEMM_OPT_TEST_STALL = 6     /* test hook for failure detection, 0 (default) or 1: the kernels with
                                    bounded waits (tensor-core GEMMs and convolution, TMA skinny GEMM) first wait on a
                                    barrier nothing arrives on; the wait runs out after the wait limit, the

@@ -205,7 +205,7 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
         h->opt_tc_chunk = (int)value;
         return GEMM_OK;
     case GEMM_OPT_TC_PAIR:
-        if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+        if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
         h->opt_tc_pair = (int)value;
         return GEMM_OK;
     case GEMM_OPT_TEST_STALL:

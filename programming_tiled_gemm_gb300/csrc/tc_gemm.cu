@@ -498,17 +498,6 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
-// Arrive on the barrier at this shared-memory offset in both CTAs of the pair once every
-// tcgen05.mma issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit_pair(uint32_t bar)
-{
-    const uint16_t both = 0x3;
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-        ::"r"(bar), "h"(both)
-        : "memory");
-}
-
 // TMA load into this CTA's shared memory whose completion is counted on a barrier that
 // may live in the peer CTA (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
@@ -521,6 +510,29 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// The same load multicast to the CTAs of `mask` (cluster ranks): the box lands at this
+// shared-memory offset in each of them, and each delivery is counted on the barrier at
+// `bar_cluster`'s offset in the even CTA of the receiving CTA's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                    int x, int y, uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
+// Arrive on the barrier at this offset in every CTA of `mask` once every tcgen05.mma
+// issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_mask(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(bar), "h"(mask)
+        : "memory");
+}
+
 // Spin (bounded by wall clock) so that copies and MMAs still in flight after an abort
 // can land before shared memory is released.
 __device__ __forceinline__ void grace_period(uint64_t ns)
@@ -530,7 +542,13 @@ __device__ __forceinline__ void grace_period(uint64_t ns)
     }
 }
 
-template <int P_STAGES>
+// PAIRS = 1: a cluster is one CTA pair computing 256 x 256 tiles.
+// PAIRS = 2: a cluster of four CTAs is two pairs computing the two 256-row halves of a
+// 512 x 256 tile.  Both pairs need the same columns of B, so each B half is read from L2
+// once for both: the CTA of each pair loads 32 of the 64 k-rows of its half and
+// multicasts them to the CTA holding the same half in the other pair.  A stage is then
+// free only when both pairs' MMAs are done with it (two arrivals on "empty").
+template <int P_STAGES, int PAIRS>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p)
 {
@@ -551,14 +569,19 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const uint32_t rank = cluster_ctarank();
-    const int pair = blockIdx.x >> 1;
-    const int npairs = gridDim.x >> 1;
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t rank = crank & 1;         // CTA within its pair
+    const int pq = (int)(crank >> 1);        // pair within the cluster
+    const uint32_t leader = crank & ~1u;     // the pair's even CTA (issues its MMAs)
+    const uint16_t pair_mask = (uint16_t)(0x3u << (2 * pq));
+    const uint16_t all_mask = (uint16_t)((1u << (2 * PAIRS)) - 1);
+    const int pair = blockIdx.x / (2 * PAIRS);   // cluster index: walks cluster tiles
+    const int npairs = gridDim.x / (2 * PAIRS);
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < P_STAGES; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), PAIRS);  // one commit per pair reading the stage
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
@@ -596,15 +619,25 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         break;
                     }
                     const uint32_t fb_local = smem_u32(&full_bar[stage]);
-                    const uint32_t fb_even = mapa_shared(fb_local, 0);
+                    const uint32_t fb_even = mapa_shared(fb_local, leader);
                     if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
                     tma_load_2d_pair(smem_u32(smem_a + stage * P_A_STAGE_BYTES), &tmA, fb_even, kb * BK,
-                                     tc.m_blk * (2 * BM) + (int)rank * BM);
+                                     (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM);
                     uint8_t* b_dst = smem_b + stage * P_B_STAGE_BYTES;
+                    if (PAIRS == 1) {
 #pragma unroll
-                    for (int j = 0; j < (BN / 2) / B_BOX_N; ++j)
-                        tma_load_2d_pair(smem_u32(b_dst + j * B_BOX_BYTES), &tmB, fb_even,
-                                         tc.n_blk * BN + (int)rank * (BN / 2) + j * B_BOX_N, kb * BK);
+                        for (int j = 0; j < (BN / 2) / B_BOX_N; ++j)
+                            tma_load_2d_pair(smem_u32(b_dst + j * B_BOX_BYTES), &tmB, fb_even,
+                                             tc.n_blk * BN + (int)rank * (BN / 2) + j * B_BOX_N, kb * BK);
+                    } else {
+                        // k-rows [32 pq, 32 pq + 32) of this CTA's B half, to both pairs
+                        const uint16_t mc = (uint16_t)((1u << rank) | (1u << (rank + 2)));
+#pragma unroll
+                        for (int j = 0; j < (BN / 2) / B_BOX_N; ++j)
+                            tma_load_2d_pair_mc(smem_u32(b_dst + j * B_BOX_BYTES + pq * (BK / 2) * 128), &tmB,
+                                                fb_even, tc.n_blk * BN + (int)rank * (BN / 2) + j * B_BOX_N,
+                                                kb * BK + pq * (BK / 2), mc);
+                    }
                     if (++stage == P_STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -650,14 +683,14 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             const uint64_t b_desc = smem_desc_sw128(b_st + k * UMMA_K * 128, B_BOX_BYTES, 1024);
                             umma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         }
-                        umma_commit_pair(smem_u32(&empty_bar[stage]));
+                        umma_commit_mask(smem_u32(&empty_bar[stage]), all_mask);  // every CTA that filled it
                         if (++stage == P_STAGES) {
                             stage = 0;
                             phase ^= 1;
                         }
                     }
                     if (!ok) break;
-                    umma_commit_pair(smem_u32(&tfull_bar[buf]));
+                    umma_commit_mask(smem_u32(&tfull_bar[buf]), pair_mask);
                     if (++buf == 2) {
                         buf = 0;
                         buf_phase ^= 1;
@@ -665,7 +698,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
             }
             if (!ok) aborted = true;
-            umma_commit_pair(smem_u32(drain_bar));  // reaches both CTAs once every MMA is done
+            umma_commit_mask(smem_u32(drain_bar), pair_mask);  // reaches both CTAs once every MMA is done
         }
         if (lane == 0) {
             if (!mbar_wait_cluster(smem_u32(drain_bar), 0, p.limit_ns, nullptr)) {
@@ -717,7 +750,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[buf]), 0));
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[buf]), leader));
                 if (++buf == 2) {
                     buf = 0;
                     buf_phase ^= 1;
@@ -728,7 +761,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 break;
             }
             const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks, p.group_m);
-            const int row = tc.m_blk * (2 * BM) + (int)rank * BM + q * 32 + lane;
+            const int row = (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM + q * 32 + lane;
             if (row < p.M && !p.epi_plain) {
                 const int col0 = tc.n_blk * BN + half * EPI_COLS;
                 const bool full = p.vec_store && col0 + EPI_COLS <= p.N;
@@ -841,35 +874,47 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.status = dev_status;
     p.limit_ns = wait_limit_ns;
     p.test_stall = a.test_stall;
-    // CTA pairs: 256 x 256 tiles on clusters of two; single CTAs: 128 x 256 tiles
-    const bool use_pair = (pair_mode == 2) || (pair_mode == 0 && a.M > BM && num_sms >= 2);
+    // CTA pairs: 256 x 256 tiles on clusters of two (or 512 x 256 tiles on clusters of
+    // two pairs sharing B); single CTAs: 128 x 256 tiles
+    const bool use_quad = (pair_mode == 3) && num_sms >= 4;
+    const bool use_pair = use_quad || (pair_mode == 2) || (pair_mode == 0 && a.M > BM && num_sms >= 2);
     if (use_pair) {
-        p.m_blocks = (int)((a.M + 2 * BM - 1) / (2 * BM));
-        const int64_t ptiles = (int64_t)p.m_blocks * p.n_blocks;
-        p.num_tiles = (int)ptiles;
+        const int pairs_per_cluster = use_quad ? 2 : 1;
+        const int cl = 2 * pairs_per_cluster;  // CTAs per cluster
+        p.m_blocks = (int)((a.M + cl * BM - 1) / (cl * BM));
+        const int64_t ctiles = (int64_t)p.m_blocks * p.n_blocks;
+        p.num_tiles = (int)ctiles;
         p.idesc = make_idesc(bf16, 2 * BM);
-        const int pairs = (int)(ptiles < num_sms / 2 ? ptiles : num_sms / 2);
-        // 6 stages of 32 KiB; 7 measured no faster.  Raster groups of 8 pair-tile rows
-        // (2048 rows of C) measured best among 2, 4, 8 and 16, within run-to-run noise.
+        const int clusters = (int)(ctiles < num_sms / cl ? ctiles : num_sms / cl);
+        // 6 stages of 32 KiB; 7 measured no faster.  Raster groups of 2048 rows of C
+        // (8 pair tiles) measured best among 512 .. 4096 rows, within run-to-run noise.
         constexpr int stages = P_STAGES_DEFAULT;
-        p.group_m = 8;
-        auto kern = tc_gemm_pair_kernel<stages>;
+        p.group_m = 8 / pairs_per_cluster;
+        CUtensorMap tmBq = tmB;
+        if (use_quad && !encode_2d(&tmBq, a.B, bf16, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.ldb, B_BOX_N, BK / 2))
+            return GEMM_ERR_CUDA;
+        auto kern = use_quad ? tc_gemm_pair_kernel<stages, 2> : tc_gemm_pair_kernel<stages, 1>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem_bytes(stages)) !=
             cudaSuccess)
             return GEMM_ERR_CUDA;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * pairs, 1, 1);
+        cfg.gridDim = dim3(cl * clusters, 1, 1);
         cfg.blockDim = dim3(THREADS, 1, 1);
         cfg.dynamicSmemBytes = p_smem_bytes(stages);
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = cl;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) return GEMM_ERR_CUDA;
+        // a persistent grid must be co-resident: clusters are placed within one GPC each,
+        // so fewer than num_sms / cl of them may fit
+        int fit = 0;
+        if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < clusters)
+            cfg.gridDim = dim3(cl * fit, 1, 1);
+        if (cudaLaunchKernelEx(&cfg, kern, tmA, use_quad ? tmBq : tmB, p) != cudaSuccess) return GEMM_ERR_CUDA;
         *launches += 1;
         return GEMM_OK;
     }

@@ -22,6 +22,7 @@ GUARD = 2
 
 PATHS = [  # (name, input dtype, M, N, K, tc pair option)
     ("tc_pair", "bf16", 520, 264, 136, 2),
+    ("tc_two_pairs", "bf16", 600, 264, 136, 3),
     ("tc_single", "f16", 300, 264, 72, 1),
     ("f32_tiled", "f32", 200, 250, 130, 0),
     ("f32_skinny", "f32", 20, 1030, 300, 0),

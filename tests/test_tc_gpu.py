@@ -70,11 +70,12 @@ SHAPES = [(1, 1, 1), (128, 256, 64), (128, 256, 16), (129, 257, 65), (200, 300, 
           (256, 512, 1024), (1000, 24, 520), (1024, 2048, 512), (2048, 4096, 384)]
 
 
-@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("pair", [1, 2, 3])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_integer_inputs_exact(lib, pair, dtype, M, N, K):
-    """pair 1: one CTA per 128 x 256 tile; pair 2: CTA pairs (cta_group::2) per 256 x 256 tile."""
+    """pair 1: one CTA per 128 x 256 tile; pair 2: CTA pairs (cta_group::2) per 256 x 256 tile;
+    pair 3: two pairs (cluster of four, B multicast) per 512 x 256 tile."""
     import programming_tiled_gemm_gb300 as g
     lib.set_option(g.GEMM_OPT_TC_PAIR, pair)
     A, B = si.integer_copy(M, N, K, seed=M + 3 * N + 7 * K, dtype=dtype)
@@ -82,7 +83,7 @@ def test_integer_inputs_exact(lib, pair, dtype, M, N, K):
     assert np.array_equal(got, oracle.gemm(A.float().numpy(), B.float().numpy()))
 
 
-@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("pair", [1, 2, 3])
 @pytest.mark.parametrize("chunk", [1, 3, 16, 4096])
 def test_accumulation_chunks_exact(lib, pair, chunk):
     import programming_tiled_gemm_gb300 as g
@@ -93,7 +94,7 @@ def test_accumulation_chunks_exact(lib, pair, chunk):
     assert np.array_equal(got, oracle.gemm(A.float().numpy(), B.float().numpy()))
 
 
-@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("pair", [1, 2, 3])
 @pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (384, 256, 4096), (200, 300, 8192)])
 def test_normal_bf16_within_tolerance(lib, pair, M, N, K):
     import programming_tiled_gemm_gb300 as g
@@ -111,10 +112,11 @@ def test_results_are_deterministic(lib):
     c1 = lib.matmul(Ad, Bd).clone()
     c2 = lib.matmul(Ad, Bd)
     assert torch.equal(c1, c2)
-    # the pair and single-CTA kernels sum the same products in the same chunk order
-    lib.set_option(g.GEMM_OPT_TC_PAIR, 1)
-    c3 = lib.matmul(Ad, Bd)
-    assert torch.equal(c1, c3)
+    # the single-CTA, pair and two-pair kernels sum the same products in the same chunk order
+    for pair in (1, 3):
+        lib.set_option(g.GEMM_OPT_TC_PAIR, pair)
+        c3 = lib.matmul(Ad, Bd)
+        assert torch.equal(c1, c3)
 
 
 def test_alignment_rules(lib):
