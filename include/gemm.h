@@ -153,13 +153,16 @@ int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t 
  *   y : fp32 [P0][P1][P2][P3][C_out], contiguous, device, Pd = in[d] - k[d] + 1;
  *       overwritten.  y[p][o] = sum over taps r and channels c of x[p + r][c] * w[o][r][c].
  * Products of 16-bit values are exact in fp32; the tensor core accumulates in fp32, with
- * consecutive 16-channel steps of the taps going round-robin to up to 8 partial sums
- * (8 for C_out = 32, 512 / (2 C_out) in general) that are added in fp32
- * round-to-nearest, in order.  Deterministic.  Asynchronous on `stream`; allocates
- * nothing.  x, w and y must be 16-byte aligned (GEMM_ERR_ALIGNMENT).
+ * consecutive MMAs (16 channels of one window of taps) going round-robin to up to 8
+ * partial sums that are added in fp32 round-to-nearest, in order.  Deterministic.
+ * Asynchronous on `stream`.  Two launches: one stages the input and the weights in the
+ * handle's workspace (grown on demand, about the size of x plus the size of w times
+ * (k[3] + 2S - 2) / k[3], S from GEMM_OPT_CONV_STACK), one computes y.
+ * x, w and y must be 16-byte aligned (GEMM_ERR_ALIGNMENT).
  * GEMM_ERR_INVALID_ARG for bad extents, pointers or dtype (GEMM_BF16 or GEMM_F16 only);
- * GEMM_ERR_UNSUPPORTED unless C_in % 16 == 0, C_out % 16 == 0, C_out <= 256,
- * in[3] <= 256, and the staged input rows of one filter row fit in shared memory. */
+ * GEMM_ERR_UNSUPPORTED unless C_in % 16 == 0, C_out % 16 == 0, S * C_out <= 256,
+ * in[3] % S == 0, and three pipeline stages of one filter triple (r0, r1, r2) fit in
+ * shared memory. */
 int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
                       int64_t C_out, const int64_t k_dims[4], float* y, int dtype, void* stream);
 
@@ -183,12 +186,15 @@ typedef enum {
     GEMM_OPT_TC_PAIR = 5,       /* tensor-core tiles: 0 choose (default: pairs when M > 128), 1 one CTA per
                                    128x256 tile, 2 a pair of CTAs (cluster of two) per 256x256 tile, 3 two
                                    pairs (cluster of four) per 512x256 tile, B read once for both pairs */
-    GEMM_OPT_TEST_STALL = 6     /* test hook for failure detection, 0 (default) or 1: the kernels with
+    GEMM_OPT_TEST_STALL = 6,    /* test hook for failure detection, 0 (default) or 1: the kernels with
                                    bounded waits (tensor-core GEMMs and convolution, TMA skinny GEMM) first wait on a
                                    barrier nothing arrives on; the wait runs out after the wait limit, the
                                    kernel drains its copies and MMAs, frees its tensor memory, returns,
                                    and gemm_get_device_status reports GEMM_ERR_DEVICE_TIMEOUT.  C is not
                                    written.  No fault, trap or unbounded wait is involved. */
+    GEMM_OPT_CONV_STACK = 7     /* tensor-core convolution (conv4d_forward_cl): output positions stacked along
+                                   the MMA's N, 0 choose (default: 2 when in[3] is even and 2*C_out <= 256,
+                                   else 1), or 1, 2, 4 */
 } gemm_option_t;
 int gemm_set_option(gemm_handle_t h, int option, int64_t value);
 

@@ -28,8 +28,9 @@ struct gemm_ctx {
     int opt_f32_kernel = 0;
     int opt_split_k = 0;
     int opt_tc_chunk = 0;  // tensor-core accumulation chunk in 64-wide k-blocks (0 = default)
-    int opt_tc_pair = 0;   // tensor-core tile: 0 choose, 1 single CTA, 2 CTA pair
+    int opt_tc_pair = 0;   // tensor-core tile: 0 choose, 1 single CTA, 2 CTA pair, 3 two pairs
     int opt_test_stall = 0;  // test hook: kernels with bounded waits let one wait run out
+    int opt_conv_stack = 0;  // tensor-core convolution: output positions stacked along N (0 = choose)
     uint64_t wait_limit_ns = 2000000000ull;
     int64_t launches = 0;  // kernels launched through this handle
     // gemm_run_host pipeline: copy-in and copy-out streams and their events
@@ -207,6 +208,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     case GEMM_OPT_TC_PAIR:
         if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
         h->opt_tc_pair = (int)value;
+        return GEMM_OK;
+    case GEMM_OPT_CONV_STACK:
+        if (value != 0 && value != 1 && value != 2 && value != 4) return GEMM_ERR_INVALID_ARG;
+        h->opt_conv_stack = (int)value;
         return GEMM_OK;
     case GEMM_OPT_TEST_STALL:
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
@@ -448,9 +453,14 @@ int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_
         return GEMM_ERR_ALIGNMENT;
     DeviceGuard g(h->device);
     if (!g.ok()) return GEMM_ERR_CUDA;
+    const int64_t ws = conv4d_tc_workspace(C_in, in_dims, C_out, k_dims, h->opt_conv_stack);
+    if (ws < 0) return GEMM_ERR_UNSUPPORTED;
+    int rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, (size_t)ws);
+    if (rc != GEMM_OK) return rc;
     int n = 0;
-    const int rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, dtype == GEMM_BF16, h->d_status,
-                                    h->wait_limit_ns, h->opt_test_stall, reinterpret_cast<cudaStream_t>(stream), &n);
+    rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, dtype == GEMM_BF16, h->opt_conv_stack, h->workspace,
+                          h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall,
+                          reinterpret_cast<cudaStream_t>(stream), &n);
     h->launches += n;
     return rc;
 }

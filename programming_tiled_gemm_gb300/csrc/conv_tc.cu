@@ -5,36 +5,42 @@
 // multiples of the MMA's K, and channel-last memory order.  With channels innermost, one
 // filter tap (r0, r1, r2, r3) times C_in channels is a contiguous run of the GEMM's K, and
 // the operand rows of that tap are input positions shifted by the tap:
-//     y[p][o] = sum_{tap} sum_c x[p + tap][c] * w[o][tap][c]
-// (p an output position, x[p + tap] the input position p0+r0, p1+r1, p2+r2, p3+r3).
+//     y[p][o] = sum_{tap} sum_c x[p + tap][c] * w[o][tap][c].
 //
-// GEMM view: M = output positions, N = C_out, K = taps x C_in.  The A operand is never
-// built, not even in shared memory: the input plane (i0, i1) = (p0 + r0, p1 + r1) is
-// staged once, by the Tensor Memory Accelerator, as a no-swizzle K-major tile (channel
-// group g of 8 channels: positions (i2, i3) row-major, 16 bytes each).  For output rows
-// q = p2 * I3 + p3 of one output plane (p0, p1), the rows for tap (r2, r3) are the staged
-// positions q + r2 * I3 + r3: 128 consecutive 16-byte rows.  So each tcgen05.mma takes
-// its A operand through a descriptor whose start address is the tap's shift; the rows
-// q with p3 >= P3 are computed too (I3 - P3 of every I3) and never stored.
-//   * tiles: 128 rows (one TMEM lane each); a plane's Q = P2 * I3 rows are covered by
-//     tiles starting at 0, 128, ..., the last one moved back to end at Q (it overlaps the
-//     previous tile; the overlap is stored once).  A CTA computes up to two tiles of one
-//     output plane, sharing every staged input plane between them.
-//   * stages: input plane (r0, r1) and a group of g2 filter rows r2 (g2 * R3 taps), with
-//     the weights of those taps: [C_out][64 k] tiles, 128-byte swizzled (TMA), the B
-//     operand (K-major, N = C_out).
-//   * accumulation: consecutive k-steps (16 channels of one tap) go round-robin to up
-//     to 8 TMEM accumulators per tile.  With N = C_out as small as 32 one MMA is short,
-//     and MMAs into the same accumulator wait for each other; independent accumulators
-//     keep the tensor core fed.  It also shortens every accumulator's sum, which matters
-//     because the tensor core's fp32 accumulator rounds toward zero; the epilogue adds
-//     the accumulators in fp32 round-to-nearest, in order.
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM owner,
-// warps 2..5 = epilogue (one per 32-lane TMEM quarter).  Every mbarrier wait is bounded
+// GEMM view.  For one i0-slab (output p0), input positions are numbered linearly over
+// (i1, i2, i3): u = (i1 * I2 + i2) * I3 + i3; output position (p1, p2, p3) is u with
+// p1 < P1, p2 < P2, p3 < P3, and tap (r1, r2, r3) of input plane i0 = p0 + r0 adds the
+// shift (r1 * I2 + r2) * I3 + r3.  So the A operand of a tap is a run of consecutive
+// staged positions, addressed by a descriptor shifted by the tap: no column matrix is
+// built anywhere.  Positions u with p1 >= P1, p2 >= P2 or p3 >= P3 are computed too and
+// never stored.
+//
+// MMA shape.  tcgen05 needs M = 128 and N >= 128 (or the shared-memory reads of A, 4 KiB
+// per MMA, bound it) to run at full rate, while N = C_out is often 32.  So S output
+// positions are stacked along N: tile row g stands for positions u0 + S g + t (t < S),
+// column block t of N (C_out wide) holds the output at offset t, and one MMA multiplies
+// the staged window at shift s by a B whose block t holds the weights of tap r3 = s - t
+// (zero outside 0..R3-1).  Windows s = r3' for r3' < R3 + S - 1 cover every tap of every
+// block; R3 / (R3 + S - 1) of the products are useful.  Window rows are S positions
+// apart, so the input is staged split by phase (u mod S): row g of window s is entry
+// (s div S) + g of phase s mod S.  The weights of one (r0, r1, r2) are staged as
+// R3 + 2S - 2 slices in reverse r3 order with zero slices at both ends, so the B of every
+// window is one contiguous run of S * C_out rows.
+//
+// Data flow.  A preparation kernel writes the phase-split input and the padded, reversed
+// weight slices into the handle's workspace (16-byte rows of 8 channels, the no-swizzle
+// K-major core-matrix layout).  The conv kernel stages, per filter triple (r0, r1, r2),
+// the input rows one tile needs and that triple's weights with contiguous bulk copies into
+// a ring of shared-memory stages; up to four threads issue the MMAs into TMEM; 4 epilogue warps
+// add the accumulators and store fp32 channel-last output.
+//   * accumulation: each issuer's MMAs go round-robin to its share of up to 8 TMEM accumulators; the
+//     tensor core's fp32 accumulator rounds toward zero, so shorter sums per accumulator
+//     keep the error small; the epilogue adds them in fp32 round-to-nearest, in order.
+// Warp roles (288 threads): warp 0 = producer, warps 1..4 = MMA issuers (lane 0 each; warp
+// 1 owns TMEM), warps 5..8 = epilogue (one per 32-lane TMEM quarter).  Every mbarrier wait is bounded
 // (wall clock); on expiry the CTA records an error in the status word, waits (bounded)
 // for its own copies and MMAs in flight, frees its TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
+#include <algorithm>
 
 #include "internal.h"
 #include "ptx.h"
@@ -42,52 +48,49 @@
 namespace gemm_gb300 {
 namespace {
 
-constexpr int CT_THREADS = 192;
-constexpr int CT_TILE_M = 128;
-constexpr int CT_MAX_TILES = 2;      // tiles of one output plane per CTA
-constexpr int CT_MAX_ACC = 8;       // TMEM accumulators per tile
-constexpr int CT_TMEM_COLS = 512;  // most TMEM columns a CTA allocates
+constexpr int CT_MAX_ISSUERS = 8;   // warps whose lane 0 issues MMAs (fewer when TMEM holds fewer accumulators)
+constexpr int CT_THREADS = 32 * (1 + CT_MAX_ISSUERS + 4);
+constexpr int CT_G = 128;           // tile rows (TMEM lanes); each stands for S positions
+constexpr int CT_MAX_ACC = 8;       // TMEM accumulators (round-robin)
+constexpr int CT_TMEM_COLS = 512;
 constexpr int CT_SMEM_BUDGET = 200 * 1024;  // pipeline stages
-constexpr int CT_MAX_STAGES = 8;
+constexpr int CT_MAX_STAGES = 12;
 
 struct ConvTcParams {
-    int cin, cout;
+    int cin, cout, S;
     int I[4], R[4], P[4];
-    int q_rows;          // Q = P2 * I3 rows per output plane
-    int tiles_per_plane;
-    int ctas_per_plane;
-    int g2;              // filter rows r2 per stage
-    int stages_per_plane;
-    int num_stages;      // R0 * R1 * stages_per_plane
-    int rows_box;        // input rows (i2) staged per channel group
-    int cg_stride;       // bytes between channel groups of the A region
-    int a_region;        // bytes of the A region (multiple of 1024)
-    int nbox_b;          // 64-wide weight boxes per stage
-    int b_box_bytes;     // C_out * 128
+    int U;              // linear positions u per i0-slab covering every valid (p1, p2, p3)
+    int tiles_per_p0;
+    int rows_box;       // staged input rows (i1, i2 merged) per tile, one filter row r2
+    int g2;             // filter rows r2 per stage (a stage: r0, r1 and g2 consecutive r2)
+    int groups;         // stages per (r0, r1): ceil(R2 / g2)
+    int xp_rows;        // merged rows per (i0, channel group, phase) block of the staged input
+    int a_blk;          // bytes of one (channel group, phase) block of a stage
+    int a_region;       // A bytes per stage, rounded up to 1024
+    int nslices;        // R3 + 2S - 2 weight slices per filter triple
+    int b_trip;         // weight bytes of one filter triple (r0, r1, r2)
     int stage_bytes;
     int nstages_ring;
-    int tx_bytes;        // bytes one stage's copies deliver
-    int nacc;            // TMEM accumulators per tile (k-steps round-robin)
-    int tmem_cols;       // allocated TMEM columns: power of two >= nacc * 2 tiles * C_out
+    int num_stages;     // R0 * R1 * groups
+    int issuers;        // MMA-issuing threads (1 .. CT_MAX_ISSUERS)
+    int nacc;           // TMEM accumulators (issuer i owns i, i + issuers, ...)
+    uint32_t acc_used;  // bit a: accumulator a receives at least one MMA
+    int s_log2;         // log2(S)
+    int tmem_cols;
     uint32_t idesc;
+    const uint8_t* xp;  // staged input (workspace)
+    const uint8_t* wp;  // staged weights (workspace)
     float* y;
     int* status;
     uint64_t limit_ns;
     int test_stall;
 };
 
-__host__ __device__ inline int tile_start(const ConvTcParams& p, int j)
-{
-    if (p.q_rows <= CT_TILE_M) return 0;
-    const int s = j * CT_TILE_M;
-    return s < p.q_rows - CT_TILE_M ? s : p.q_rows - CT_TILE_M;
-}
-
-// kind::f16 instruction descriptor: fp32 accumulator, A and B K-major, M = 128, N = C_out.
+// kind::f16 instruction descriptor: fp32 accumulator, A and B K-major, M = 128, N = n.
 __host__ inline uint32_t conv_idesc(bool bf16, int n)
 {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(CT_TILE_M >> 4) << 24);
+           ((uint32_t)(CT_G >> 4) << 24);
 }
 
 __device__ __forceinline__ void ct_record_error(int* status, int code, volatile int* abort_flag)
@@ -96,9 +99,48 @@ __device__ __forceinline__ void ct_record_error(int* status, int code, volatile 
     *abort_flag = 1;
 }
 
-__global__ void __launch_bounds__(CT_THREADS, 1)
-conv4d_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                 ConvTcParams p)
+// Staged operands, in 16-byte chunks of 8 channels:
+//   xp[i0][g][phase][row][m]   = x[i0][row / I2][row % I2][phase + S m][8 g .. 8 g + 7]
+//                                (zero for row >= I1 * I2; rows 0 .. xp_rows - 1)
+//   wp[trip][g][j][o]          = w[o][r0][r1][r2][R3 + S - 2 - j][8 g .. 8 g + 7]
+//                                (zero when that r3 is outside 0 .. R3 - 1)
+//   grid.y < I0 * C_in/8 * S: one (i0, g, phase) block of xp per y, rows x entries along x;
+//   the rest of grid.y: one filter triple's weights per y.
+__global__ void __launch_bounds__(256)
+conv_tc_prepare_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w, ConvTcParams p, uint4* xp, uint4* wp)
+{
+    const int cg = p.cin / 8;
+    const int mS = p.I[3] / p.S;
+    const int nblk = p.I[0] * cg * p.S;
+    const int by = blockIdx.y;
+    if (by < nblk) {
+        const int ph = by % p.S, g = (by / p.S) % cg, i0 = by / (p.S * cg);
+        const int plane_rows = p.I[1] * p.I[2];
+        const int n = p.xp_rows * mS;
+        uint4* dst = xp + (int64_t)by * n;
+        const uint4* src = x + (int64_t)i0 * plane_rows * p.I[3] * cg + g;
+        for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
+            const int row = e / mS, m = e - row * mS;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (row < plane_rows) v = src[((int64_t)row * p.I[3] + ph + p.S * m) * cg];
+            dst[e] = v;
+        }
+    } else {
+        const int trip = by - nblk;
+        const int trips = p.R[0] * p.R[1] * p.R[2];
+        const int n = cg * p.nslices * p.cout;  // (g, j, o) of this triple
+        uint4* dst = wp + (int64_t)trip * n;
+        for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
+            const int o = e % p.cout, j = (e / p.cout) % p.nslices, g = e / (p.cout * p.nslices);
+            const int r3 = p.R[3] + p.S - 2 - j;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r3 >= 0 && r3 < p.R[3]) v = w[(((int64_t)o * trips + trip) * p.R[3] + r3) * cg + g];
+            dst[e] = v;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(CT_THREADS, 1) conv4d_tc_kernel(ConvTcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -116,26 +158,23 @@ conv4d_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    // this CTA: output plane (p0, p1) and its tiles [t0, t0 + ntile)
-    const int plane = blockIdx.x / p.ctas_per_plane;
-    const int cta_in_plane = blockIdx.x % p.ctas_per_plane;
-    const int p0 = plane / p.P[1], p1 = plane % p.P[1];
-    const int t0 = cta_in_plane * CT_MAX_TILES;
-    const int ntile = min(CT_MAX_TILES, p.tiles_per_plane - t0);
-    const int row0 = tile_start(p, t0) / p.I[3];  // first staged input row (before r2)
+    // this CTA: output slab p0, positions u0 .. u0 + 128 S - 1
+    const int p0 = blockIdx.x / p.tiles_per_p0;
+    const int u0 = (blockIdx.x % p.tiles_per_p0) * CT_G * p.S;
+    const int row0 = u0 / p.I[3];            // first staged row before the tap's row shift
+    const int col0 = u0 - row0 * p.I[3];     // a multiple of S
+    const int N = p.S * p.cout;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < SA; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), (uint32_t)p.issuers);  // one commit per issuer
         }
-        mbar_init(smem_u32(done_bar), 1);
-        mbar_init(smem_u32(drain_bar), 1);
+        mbar_init(smem_u32(done_bar), (uint32_t)p.issuers);
+        mbar_init(smem_u32(drain_bar), (uint32_t)p.issuers);
         mbar_init(smem_u32(never_bar), 1);
         *abort_flag = 0;
         mbar_fence_init();
-        prefetch_tensormap(&tmX);
-        prefetch_tensormap(&tmW);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), (uint32_t)p.tmem_cols);
@@ -150,28 +189,41 @@ conv4d_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             uint32_t issued_mask = 0, last_parity = 0;
+            const int64_t row_bytes = (int64_t)(p.I[3] / p.S) * 16;
+            const int64_t blk_stride = (int64_t)p.xp_rows * row_bytes;  // one (i0, g, phase) block
+            int slot = 0, r0 = 0, r1 = 0, grp = 0;
+            uint32_t ph = 0;
             for (int st = 0; st < p.num_stages; ++st) {
-                const int slot = st % SA;
-                const uint32_t ph = (uint32_t)(st / SA) & 1;
-                if (*abort_flag || !mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1, p.limit_ns, abort_flag)) {
+                if (*abort_flag || !mbar_wait_sleep(smem_u32(&empty_bar[slot]), ph ^ 1, p.limit_ns, abort_flag, 200)) {
                     ct_record_error(p.status, kDevTimeoutProducer, abort_flag);
                     break;
                 }
-                const int pi = st / p.stages_per_plane;
-                const int r0 = pi / p.R[1], r1 = pi % p.R[1];
-                const int r2s = (st % p.stages_per_plane) * p.g2;
+                const int r2s = grp * p.g2;
+                const int g = min(p.g2, p.R[2] - r2s);
+                const int row = row0 + r1 * p.I[2] + r2s;
+                // the rows of g filter rows: rows_box + g - 1 (a short last group copies fewer)
+                const uint32_t a_bytes = (uint32_t)((p.rows_box + g - 1) * row_bytes);
                 const uint32_t fb = smem_u32(&full_bar[slot]);
-                mbar_arrive_expect_tx(fb, (uint32_t)p.tx_bytes);
+                mbar_arrive_expect_tx(fb, (uint32_t)(cgroups * p.S) * a_bytes + (uint32_t)(g * p.b_trip));
                 uint8_t* a_dst = smem + slot * p.stage_bytes;
-                const int plane_in = (p0 + r0) * p.I[1] + (p1 + r1);
-                for (int g = 0; g < cgroups; ++g)
-                    tma_load_5d(smem_u32(a_dst + g * p.cg_stride), &tmX, fb, 0, g, 0, row0 + r2s, plane_in);
-                uint8_t* b_dst = a_dst + p.a_region;
-                const int k0 = ((pi * p.R[2] + r2s) * p.R[3]) * p.cin;
-                for (int b = 0; b < p.nbox_b; ++b)
-                    tma_load_2d(smem_u32(b_dst + b * p.b_box_bytes), &tmW, fb, k0 + 64 * b, 0);
+                const uint8_t* src = p.xp + ((int64_t)(p0 + r0) * cgroups * p.S) * blk_stride + row * row_bytes;
+                for (int b = 0; b < cgroups * p.S; ++b)
+                    bulk_load(smem_u32(a_dst + b * p.a_blk), src + b * blk_stride, a_bytes, fb);
+                const int64_t trip = ((int64_t)r0 * p.R[1] + r1) * p.R[2] + r2s;
+                bulk_load(smem_u32(a_dst + p.a_region), p.wp + trip * p.b_trip, (uint32_t)(g * p.b_trip), fb);
                 issued_mask |= 1u << slot;
                 last_parity = (last_parity & ~(1u << slot)) | (ph << slot);
+                if (++slot == SA) {
+                    slot = 0;
+                    ph ^= 1;
+                }
+                if (++grp == p.groups) {
+                    grp = 0;
+                    if (++r1 == p.R[1]) {
+                        r1 = 0;
+                        ++r0;
+                    }
+                }
             }
             // every copy this CTA issued must have landed before its shared memory goes away
             for (int s = 0; s < SA; ++s)
@@ -180,58 +232,77 @@ conv4d_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                         ct_record_error(p.status, kDevTimeoutDrain, abort_flag);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+    } else if (warp <= CT_MAX_ISSUERS) {
+        // ---------------------------------------------------------------- MMA issuers
+        // The (filter row, window) pairs of a stage are dealt round-robin to the issuers;
+        // issuer i uses the accumulators i, i + issuers, ... in turn.  One thread issues
+        // at best about one MMA per 55 cycles, while an MMA with N = 64 or 128 takes
+        // 32 to 64, so several threads issue.
+        if (lane == 0 && warp - 1 < p.issuers) {
+            const int issuer = warp - 1;
+            const int T = p.issuers;
             bool ok = true;
             const int ksteps = p.cin / 16;
-            const bool two = ntile > 1;
-            // tile row offsets inside the staged rows, in 16-byte positions; descriptors
-            // hold the start address in 16-byte units in their low bits, so moving an
-            // operand by n positions is adding n to its descriptor (no carry: shared
-            // memory addresses stay below 2^18 bytes)
-            const uint32_t qoff0 = (uint32_t)(tile_start(p, t0) - row0 * p.I[3]);
-            const uint32_t qoff1 = two ? (uint32_t)(tile_start(p, t0 + 1) - row0 * p.I[3]) : 0u;
-            const uint32_t cg2 = (uint32_t)(2 * p.cg_stride) >> 4;  // next 16 channels of A
-            const uint32_t box16 = (uint32_t)p.b_box_bytes >> 4;    // next 64-wide weight box
-            const uint32_t acc_cols = (uint32_t)(CT_MAX_TILES * p.cout);  // TMEM columns per accumulator
-            uint32_t kstep = 0, acc_idx = 0;
+            const int windows = p.R[3] + p.S - 1;
+            // Descriptors hold the start address in 16-byte units in their low bits, so
+            // moving an operand by n 16-byte rows is adding n to its descriptor (no carry:
+            // shared-memory addresses stay below 2^18 bytes).
+            const uint32_t a_cg2 = (uint32_t)(2 * p.S * p.a_blk) >> 4;            // next 16 channels of A
+            const uint32_t b_cg2 = (uint32_t)(2 * p.nslices * p.cout * 16) >> 4;  // next 16 channels of B
+            const uint32_t a_phase = (uint32_t)p.a_blk >> 4;                      // next phase of A
+            const uint32_t a_row = (uint32_t)(p.I[3] / p.S);                      // next input row (r2 + 1)
+            const uint32_t b_slice = (uint32_t)p.cout;                            // one weight slice
+            const uint32_t b_r2 = (uint32_t)p.b_trip >> 4;                        // next filter triple
+            const uint32_t acc_cols = (uint32_t)N;
+            const uint32_t my_acc = (uint32_t)(p.nacc / T);
+            uint32_t mma = 0, acc_j = 0;
+            int slot = 0, grp = 0;
+            uint32_t ph = 0;
             for (int st = 0; st < p.num_stages; ++st) {
-                const int slot = st % SA;
-                const uint32_t ph = (uint32_t)(st / SA) & 1;
                 if (*abort_flag || !mbar_wait(smem_u32(&full_bar[slot]), ph, p.limit_ns, abort_flag)) {
                     ct_record_error(p.status, kDevTimeoutMma, abort_flag);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int r2s = (st % p.stages_per_plane) * p.g2;
-                const int g = min(p.g2, p.R[2] - r2s);
+                const int g = min(p.g2, p.R[2] - grp * p.g2);
                 const uint32_t a_st = smem_u32(smem + slot * p.stage_bytes);
-                const uint64_t a_desc0 = smem_desc(a_st, (uint32_t)p.cg_stride, 128, kLayoutNoSwizzle);
-                uint64_t b_box = smem_desc_sw128(a_st + p.a_region, 16, 1024);  // current weight box
-                uint32_t b_step = 0;                                            // 16-k step inside it
-                for (int rr = 0; rr < g; ++rr) {
-                    for (int r3 = 0; r3 < p.R[3]; ++r3) {
-                        // position shift of tap (r2s + rr, r3)
-                        uint64_t a_desc = a_desc0 + (uint32_t)(rr * p.I[3] + r3);
-                        for (int s = 0; s < ksteps; ++s) {
-                            const uint64_t b_desc = b_box + 2 * b_step;  // 32 bytes per step
-                            const uint32_t d0 = tmem_base + acc_idx * acc_cols;
-                            const uint32_t acc = kstep >= (uint32_t)p.nacc ? 1u : 0u;  // first use overwrites
-                            umma_f16(d0, a_desc + qoff0, b_desc, p.idesc, acc);
-                            if (two) umma_f16(d0 + (uint32_t)p.cout, a_desc + qoff1, b_desc, p.idesc, acc);
-                            ++kstep;
-                            if (++acc_idx == (uint32_t)p.nacc) acc_idx = 0;
-                            a_desc += cg2;
-                            if (++b_step == 4) {
-                                b_step = 0;
-                                b_box += box16;
-                            }
-                        }
+                const uint64_t a_r = smem_desc(a_st + (uint32_t)(col0 / p.S) * 16, (uint32_t)(p.S * p.a_blk), 128,
+                                               kLayoutNoSwizzle);
+                // window 0 takes the slices from R3 + S - 2 on; window s starts s slices earlier
+                const uint64_t b_r = smem_desc(a_st + p.a_region + (uint32_t)((p.R[3] + p.S - 2) * p.cout * 16),
+                                               (uint32_t)(p.nslices * p.cout * 16), 128, kLayoutNoSwizzle);
+                // pairs (rr, s), s fastest; this issuer starts at pair `issuer` and steps by T
+                int rr = 0, s = issuer;
+                while (s >= windows) {
+                    s -= windows;
+                    ++rr;
+                }
+                while (rr < g) {
+                    // window s of filter row rr: phase s mod S, (s div S) entries on; B s slices earlier
+                    const uint64_t a_w = a_r + (uint32_t)rr * a_row + (uint32_t)(s & (p.S - 1)) * a_phase +
+                                         (uint32_t)(s >> p.s_log2);
+                    const uint64_t b_w = b_r + (uint32_t)rr * b_r2 - (uint64_t)((uint32_t)s * b_slice);
+                    for (int k = 0; k < ksteps; ++k) {
+                        const uint32_t acc = mma >= my_acc ? 1u : 0u;  // first use overwrites
+                        const uint32_t a_idx = (uint32_t)issuer + acc_j * (uint32_t)T;
+                        umma_f16(tmem_base + a_idx * acc_cols, a_w + (uint32_t)k * a_cg2, b_w + (uint32_t)k * b_cg2,
+                                 p.idesc, acc);
+                        ++mma;
+                        if (++acc_j == my_acc) acc_j = 0;
+                    }
+                    s += T;
+                    while (s >= windows) {
+                        s -= windows;
+                        ++rr;
                     }
                 }
                 umma_commit(smem_u32(&empty_bar[slot]));  // stage free once these MMAs finish
+                if (++slot == SA) {
+                    slot = 0;
+                    ph ^= 1;
+                }
+                if (++grp == p.groups) grp = 0;
             }
             if (ok) umma_commit(smem_u32(done_bar));
             // no MMA of this CTA may still be running when TMEM and shared memory are released
@@ -251,40 +322,35 @@ conv4d_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             if (!ok && lane == 0) ct_record_error(p.status, kDevTimeoutEpilogue, abort_flag);
         }
         if (ok) {
-            ok = mbar_wait(smem_u32(done_bar), 0, p.limit_ns, abort_flag);
+            ok = mbar_wait_sleep(smem_u32(done_bar), 0, p.limit_ns, abort_flag, 1000);  // waits the whole main loop
             ok = __all_sync(0xffffffffu, ok);
             if (!ok && lane == 0) ct_record_error(p.status, kDevTimeoutEpilogue, abort_flag);
         }
         if (ok) {
             tc_fence_after();
-            const int r = quarter * 32 + lane;  // tile row of this thread
-            const int P23 = p.P[2] * p.P[3];
-            float* yplane = p.y + ((int64_t)plane * P23) * p.cout;
-            for (int j = 0; j < ntile; ++j) {
-                const int t = t0 + j;
-                const int q = tile_start(p, t) + r;
-                const int q_min = (t == 0) ? 0 : tile_start(p, t - 1) + CT_TILE_M;  // rows of earlier tiles
-                const int p2 = q / p.I[3], p3 = q % p.I[3];
-                const bool store = q < p.q_rows && q >= q_min && p3 < p.P[3];
-                float* yrow = yplane + ((int64_t)p2 * p.P[3] + p3) * p.cout;
-                for (int c0 = 0; c0 < p.cout; c0 += 16) {
-                    float acc[16];
-                    for (int a = 0; a < p.nacc; ++a) {  // accumulators in fixed order
-                        uint32_t v[16];
-                        tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                                               (uint32_t)((a * CT_MAX_TILES + j) * p.cout + c0),
-                                           v);
-                        tmem_ld_wait();
+            const int g = quarter * 32 + lane;  // tile row of this thread
+            const int plane = p.I[2] * p.I[3];
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                float acc[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[i] = (a == 0) ? __uint_as_float(v[i]) : __fadd_rn(acc[i], __uint_as_float(v[i]));
-                    }
-                    if (store) {
+                for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                for (int a = 0; a < p.nacc; ++a) {  // the accumulators that received MMAs, in order
+                    if (!((p.acc_used >> a) & 1)) continue;
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * N + c0), v);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; i += 4)
-                            *reinterpret_cast<float4*>(yrow + c0 + i) =
-                                make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-                    }
+                    for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __uint_as_float(v[i]));
+                }
+                const int t = c0 / p.cout, o0 = c0 % p.cout;
+                const int u = u0 + g * p.S + t;
+                const int p1 = u / plane, rem = u - p1 * plane;
+                const int p2 = rem / p.I[3], p3 = rem - p2 * p.I[3];
+                if (p1 < p.P[1] && p2 < p.P[2] && p3 < p.P[3]) {
+                    float* yrow = p.y + ((((int64_t)p0 * p.P[1] + p1) * p.P[2] + p2) * p.P[3] + p3) * p.cout + o0;
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4)
+                        *reinterpret_cast<float4*>(yrow + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
                 }
             }
         }
@@ -298,122 +364,162 @@ conv4d_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     }
 }
 
-}  // namespace
-
-int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void* w, int64_t cout,
-                     const int64_t k[4], float* y, bool bf16, int* dev_status, uint64_t limit_ns, int test_stall,
-                     cudaStream_t stream, int* launches)
+// Plan of a launch: fills everything but the pointers.  Returns a gemm_status_t.
+int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S, ConvTcParams* out)
 {
-    if (cin % 16 != 0 || cout % 16 != 0 || cout < 16 || cout > 256) return GEMM_ERR_UNSUPPORTED;
+    if (cin % 16 != 0 || cout % 16 != 0 || cout < 16 || cout > 256 || cin > 2048) return GEMM_ERR_UNSUPPORTED;
+    if ((S != 1 && S != 2 && S != 4) || S * cout > 256 || in[3] % S != 0) return GEMM_ERR_UNSUPPORTED;
     ConvTcParams p = {};
-    int64_t P[4];
-    for (int d = 0; d < 4; ++d) {
-        P[d] = in[d] - k[d] + 1;
-        if (in[d] > (1 << 20) || k[d] > (1 << 20)) return GEMM_ERR_UNSUPPORTED;
-        p.I[d] = (int)in[d];
-        p.R[d] = (int)k[d];
-        p.P[d] = (int)P[d];
-    }
-    const int64_t taps = k[0] * k[1] * k[2] * k[3];
-    const int64_t K = taps * cin;
-    const int64_t planes_out = P[0] * P[1];
-    const int64_t Q = P[2] * in[3];
-    if (in[3] > 256 || K >= (1ll << 31) || in[0] * in[1] >= (1ll << 31) || Q >= (1 << 30) || cin > 2048)
-        return GEMM_ERR_UNSUPPORTED;
     p.cin = (int)cin;
     p.cout = (int)cout;
-    p.q_rows = (int)Q;
-    p.tiles_per_plane = (int)((Q + CT_TILE_M - 1) / CT_TILE_M);
-    p.ctas_per_plane = (p.tiles_per_plane + CT_MAX_TILES - 1) / CT_MAX_TILES;
-    const int64_t grid = planes_out * p.ctas_per_plane;
-    if (grid >= (1ll << 31)) return GEMM_ERR_UNSUPPORTED;
-    p.b_box_bytes = (int)cout * 128;
-
-    // largest r2 group whose stage leaves room for at least three stages; the staged
-    // input rows must cover every tile's rows shifted by every tap of the group
-    int chosen = 0;
-    for (int g2 = (int)k[2]; g2 >= 1 && !chosen; --g2) {
-        int rows_box = 0;
-        for (int c = 0; c < p.ctas_per_plane; ++c) {
-            const int t0 = c * CT_MAX_TILES;
-            const int tl = (t0 + CT_MAX_TILES < p.tiles_per_plane ? t0 + CT_MAX_TILES : p.tiles_per_plane) - 1;
-            const int row0 = tile_start(p, t0) / p.I[3];
-            const int64_t span = (int64_t)tile_start(p, tl) - (int64_t)row0 * in[3] + CT_TILE_M +
-                                 (int64_t)(g2 - 1) * in[3] + (k[3] - 1);
-            const int64_t rows = (span + in[3] - 1) / in[3];
-            if (rows > rows_box) rows_box = (int)(rows > (1 << 20) ? (1 << 20) : rows);
-        }
-        if (rows_box > 256) continue;
-        const int64_t cg_bytes = (int64_t)rows_box * in[3] * 16;
-        const int64_t cg_stride = (cg_bytes + 127) / 128 * 128;
-        const int64_t a_region = ((cin / 8) * cg_stride + 1023) / 1024 * 1024;
-        const int64_t nbox_b = ((int64_t)g2 * k[3] * cin + 63) / 64;
-        const int64_t stage = a_region + nbox_b * p.b_box_bytes;
-        if (3 * stage > CT_SMEM_BUDGET) continue;
-        p.g2 = g2;
-        p.rows_box = rows_box;
-        p.cg_stride = (int)cg_stride;
-        p.a_region = (int)a_region;
-        p.nbox_b = (int)nbox_b;
-        p.stage_bytes = (int)stage;
-        p.tx_bytes = (int)((cin / 8) * cg_bytes + nbox_b * p.b_box_bytes);
-        chosen = 1;
+    p.S = S;
+    for (int d = 0; d < 4; ++d) {
+        if (in[d] > (1 << 20) || k[d] > in[d]) return GEMM_ERR_UNSUPPORTED;
+        p.I[d] = (int)in[d];
+        p.R[d] = (int)k[d];
+        p.P[d] = (int)(in[d] - k[d] + 1);
     }
-    if (!chosen) return GEMM_ERR_UNSUPPORTED;
-    p.stages_per_plane = (p.R[2] + p.g2 - 1) / p.g2;
-    const int64_t nst = k[0] * k[1] * p.stages_per_plane;
-    if (nst >= (1ll << 30)) return GEMM_ERR_UNSUPPORTED;
+    const int64_t plane = in[2] * in[3];
+    const int64_t U = (int64_t)p.P[1] * plane;
+    const int64_t tile_pos = (int64_t)CT_G * S;
+    const int64_t tiles = (U + tile_pos - 1) / tile_pos;
+    const int64_t grid = tiles * p.P[0];
+    if (U >= (1ll << 30) || grid >= (1ll << 31) || in[0] * in[1] * in[2] * in[3] >= (1ll << 31))
+        return GEMM_ERR_UNSUPPORTED;
+    p.U = (int)U;
+    p.tiles_per_p0 = (int)tiles;
+    // staged rows: a tile's positions plus the largest window shift R3 + S - 2, from the
+    // tile's first row; the tile start within its row is a multiple of S below I3
+    int64_t rows_box = 0;
+    if (tiles <= 4096) {
+        for (int64_t t = 0; t < tiles; ++t) {
+            const int64_t span = ((t * tile_pos) % in[3]) + tile_pos + (k[3] + S - 2);
+            const int64_t rows = (span + in[3] - 1) / in[3];
+            if (rows > rows_box) rows_box = rows;
+        }
+    } else {
+        rows_box = ((in[3] - S) + tile_pos + (k[3] + S - 2) + in[3] - 1) / in[3];
+    }
+    p.rows_box = (int)rows_box;
+    // merged rows the last tile may reach: its first row, the largest tap row shift
+    // (R1 - 1) I2 + R2 - 1, and the staged rows
+    const int64_t last_row = (tiles - 1) * tile_pos / in[3] + (k[1] - 1) * in[2] + (k[2] - 1) + rows_box;
+    if (last_row >= (1ll << 30)) return GEMM_ERR_UNSUPPORTED;
+    p.xp_rows = (int)(last_row > in[1] * in[2] ? last_row : in[1] * in[2]);
+    // the staging kernel: 32-bit indices within a block, one grid row per block and triple
+    if ((int64_t)p.xp_rows * (in[3] / S) >= (1ll << 31) ||
+        in[0] * (cin / 8) * S + k[0] * k[1] * k[2] > 65535)
+        return GEMM_ERR_UNSUPPORTED;
+    p.nslices = (int)(k[3] + 2 * S - 2);
+    p.b_trip = (int)((cin / 8) * p.nslices * cout * 16);
+    // MMA issuers: one per pair of TMEM accumulators' share, at most CT_MAX_ISSUERS
+    const int N = S * p.cout;
+    int nacc = CT_TMEM_COLS / N;
+    if (nacc > CT_MAX_ACC) nacc = CT_MAX_ACC;
+    p.issuers = nacc < CT_MAX_ISSUERS ? nacc : CT_MAX_ISSUERS;
+    nacc -= nacc % p.issuers;
+    p.nacc = nacc;
+    const int64_t windows = k[3] + S - 1;
+    // the most filter rows r2 per stage that leave room for three stages
+    p.g2 = 0;
+    for (int64_t g2 = k[2]; g2 >= 1 && p.g2 == 0; --g2) {
+        const int64_t a_blk = (rows_box + g2 - 1) * (in[3] / S) * 16;
+        const int64_t a_region = ((cin / 8) * S * a_blk + 1023) / 1024 * 1024;
+        const int64_t stage = (a_region + g2 * p.b_trip + 1023) / 1024 * 1024;
+        if (3 * stage > CT_SMEM_BUDGET) continue;
+        p.g2 = (int)g2;
+        p.a_blk = (int)a_blk;
+        p.a_region = (int)a_region;
+        p.stage_bytes = (int)stage;
+    }
+    if (p.g2 == 0) return GEMM_ERR_UNSUPPORTED;
+    p.groups = (p.R[2] + p.g2 - 1) / p.g2;
+    const int64_t nst = k[0] * k[1] * p.groups;
+    if (nst >= (1 << 30) || k[0] * k[1] * k[2] >= (1 << 30)) return GEMM_ERR_UNSUPPORTED;
     p.num_stages = (int)nst;
     int ring = CT_SMEM_BUDGET / p.stage_bytes;
     if (ring > CT_MAX_STAGES) ring = CT_MAX_STAGES;
     if (ring > p.num_stages) ring = p.num_stages;
     p.nstages_ring = ring;
-    const int64_t ksteps = taps * (cin / 16);
-    int nacc = CT_TMEM_COLS / (CT_MAX_TILES * p.cout);
-    if (nacc > CT_MAX_ACC) nacc = CT_MAX_ACC;
-    if (nacc > ksteps) nacc = (int)ksteps;
-    p.nacc = nacc;
+    // accumulator i + issuers j is written iff issuer i issues more than j MMAs; issuer i
+    // takes (row, window) pairs i, i + issuers, ... of every stage
+    p.acc_used = 0;
+    for (int a = 0; a < nacc; ++a) {
+        const int issuer = a % p.issuers, j = a / p.issuers;
+        int64_t mine = 0;
+        for (int grp = 0; grp < p.groups; ++grp) {
+            const int64_t pairs = (int64_t)(p.R[2] - grp * p.g2 < p.g2 ? p.R[2] - grp * p.g2 : p.g2) * windows;
+            mine += pairs > issuer ? (pairs - issuer + p.issuers - 1) / p.issuers : 0;
+        }
+        if (mine * k[0] * k[1] * (cin / 16) > j) p.acc_used |= 1u << a;
+    }
+    p.s_log2 = (S == 4) ? 2 : (S == 2) ? 1 : 0;
     p.tmem_cols = 32;
-    while (p.tmem_cols < nacc * CT_MAX_TILES * p.cout) p.tmem_cols *= 2;
-    p.idesc = conv_idesc(bf16, p.cout);
+    while (p.tmem_cols < nacc * N) p.tmem_cols *= 2;
+    *out = p;
+    return GEMM_OK;
+}
+
+// Positions stacked along N: 2 when the shape allows it, else 1.
+int choose_stack(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4])
+{
+    ConvTcParams p;
+    for (int S : {2, 1})
+        if (plan_conv4d_tc(cin, in, cout, k, S, &p) == GEMM_OK) return S;
+    return 0;
+}
+
+int64_t staged_input_bytes(const ConvTcParams& p)
+{
+    return (int64_t)p.I[0] * (p.cin / 8) * p.S * p.xp_rows * (p.I[3] / p.S) * 16;
+}
+
+}  // namespace
+
+int64_t conv4d_tc_workspace(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S)
+{
+    ConvTcParams p;
+    if (S <= 0) S = choose_stack(cin, in, cout, k);
+    if (S <= 0 || plan_conv4d_tc(cin, in, cout, k, S, &p) != GEMM_OK) return -1;
+    return staged_input_bytes(p) + (int64_t)p.R[0] * p.R[1] * p.R[2] * p.b_trip;
+}
+
+int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void* w, int64_t cout,
+                     const int64_t k[4], float* y, bool bf16, int S, void* workspace, int num_sms, int* dev_status,
+                     uint64_t limit_ns, int test_stall, cudaStream_t stream, int* launches)
+{
+    if (S <= 0) S = choose_stack(cin, in, cout, k);
+    if (S <= 0) return GEMM_ERR_UNSUPPORTED;
+    ConvTcParams p;
+    const int rc = plan_conv4d_tc(cin, in, cout, k, S, &p);
+    if (rc != GEMM_OK) return rc;
+    const int64_t xb = staged_input_bytes(p);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.xp = ws;
+    p.wp = ws + xb;
+    p.idesc = conv_idesc(bf16, S * p.cout);
     p.y = y;
     p.status = dev_status;
     p.limit_ns = limit_ns;
     p.test_stall = test_stall;
 
-    // x as [plane = i0*I1 + i1][i2][i3][channel group][8 channels]: one box = one
-    // channel group of `rows_box` input rows (zero fill past I2)
-    auto enc = tensor_map_encoder();
-    if (!enc) return GEMM_ERR_CUDA;
-    const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap tmX, tmW;
-    {
-        cuuint64_t dims[5] = {8, (cuuint64_t)(cin / 8), (cuuint64_t)in[3], (cuuint64_t)in[2],
-                              (cuuint64_t)(in[0] * in[1])};
-        cuuint64_t strides[4] = {16, (cuuint64_t)cin * 2, (cuuint64_t)(in[3] * cin * 2),
-                                 (cuuint64_t)(in[2] * in[3] * cin * 2)};
-        cuuint32_t box[5] = {8, 1, (cuuint32_t)in[3], (cuuint32_t)p.rows_box, 1};
-        cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-        if (enc(&tmX, dt, 5, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return GEMM_ERR_CUDA;
-    }
-    {
-        // w as the row-major [C_out][K] matrix; box = 64 k x C_out rows, 128-byte swizzle
-        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)cout};
-        cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        cuuint32_t box[2] = {64, (cuuint32_t)cout};
-        cuuint32_t estr[2] = {1, 1};
-        if (enc(&tmW, dt, 2, const_cast<void*>(w), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return GEMM_ERR_CUDA;
-    }
+    // one grid row per staged-input block and per filter triple, enough blocks along x
+    // for about 4 waves in all
+    const int64_t nblk = (int64_t)p.I[0] * (cin / 8) * S;
+    const int64_t rows_y = nblk + (int64_t)p.R[0] * p.R[1] * p.R[2];
+    const int64_t per_y = std::max<int64_t>((int64_t)p.xp_rows * (p.I[3] / S), (cin / 8) * p.nslices * cout);
+    int64_t gx = (int64_t)num_sms * 4 * 8 / rows_y;  // 8 blocks of 256 threads per SM
+    gx = std::min<int64_t>(std::max<int64_t>(gx, 1), (per_y + 255) / 256);
+    conv_tc_prepare_kernel<<<dim3((unsigned)gx, (unsigned)rows_y), 256, 0, stream>>>(
+        static_cast<const uint4*>(x), static_cast<const uint4*>(w), p, reinterpret_cast<uint4*>(ws),
+        reinterpret_cast<uint4*>(ws + xb));
+    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+    *launches += 1;
+
     const int smem = p.nstages_ring * p.stage_bytes + 1024 /*barriers*/ + 1024 /*alignment slack*/;
     if (cudaFuncSetAttribute(conv4d_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GEMM_ERR_CUDA;
-    conv4d_tc_kernel<<<(unsigned)grid, CT_THREADS, smem, stream>>>(tmX, tmW, p);
+    conv4d_tc_kernel<<<(unsigned)(p.tiles_per_p0 * p.P[0]), CT_THREADS, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
     *launches += 1;
     return GEMM_OK;

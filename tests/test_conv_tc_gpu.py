@@ -63,7 +63,7 @@ def int_operands(cin, cout, ins, ks, seed, dtype="bf16"):
     return si.channel_last(x, w, dtype)
 
 
-SHAPES = [  # (C_in, C_out, input extents, kernel extents)
+SHAPES = [  # (C_in, C_out, input extents, kernel extents); odd in[3] or 2 C_out > 256 run unstacked
     (16, 32, (6, 5, 16, 16), (3, 2, 5, 5)),     # two tiles per plane, one CTA
     (32, 48, (5, 6, 7, 9), (2, 3, 2, 4)),       # two 16-channel steps per tap, one tile
     (16, 16, (3, 3, 20, 30), (1, 2, 3, 3)),     # five tiles per plane over three CTAs
@@ -79,6 +79,31 @@ SHAPES = [  # (C_in, C_out, input extents, kernel extents)
 def test_integer_inputs_are_exact(lib, cin, cout, ins, ks):
     x, w = int_operands(cin, cout, ins, ks, seed=cin + cout + sum(ins))
     assert np.array_equal(run_guarded(lib, x, w), conv_ref(x, w))
+
+
+STACKED = [  # (stack S, C_in, C_out, input extents, kernel extents): S | in[3], S C_out <= 256
+    (1, 16, 32, (6, 5, 16, 16), (3, 2, 5, 5)),
+    (2, 16, 32, (6, 5, 16, 16), (3, 2, 5, 5)),
+    (4, 16, 32, (6, 5, 16, 16), (3, 2, 5, 5)),
+    (2, 32, 48, (5, 6, 7, 10), (2, 3, 2, 4)),
+    (2, 16, 16, (3, 3, 20, 30), (1, 2, 3, 3)),
+    (4, 16, 64, (3, 3, 9, 12), (2, 1, 4, 5)),
+    (2, 16, 128, (2, 2, 4, 4), (1, 1, 2, 2)),
+    (4, 16, 32, (7, 7, 7, 8), (7, 7, 7, 7)),
+]
+
+
+@pytest.mark.parametrize("stack,cin,cout,ins,ks", STACKED)
+def test_stacked_positions_are_exact(lib, stack, cin, cout, ins, ks):
+    """S output positions per tile row, stacked along the MMA's N (GEMM_OPT_CONV_STACK)."""
+    import programming_tiled_gemm_gb300 as g
+    x, w = int_operands(cin, cout, ins, ks, seed=7 * stack + cin + sum(ks))
+    lib.set_option(g.GEMM_OPT_CONV_STACK, stack)
+    try:
+        got = run_guarded(lib, x, w)
+    finally:
+        lib.set_option(g.GEMM_OPT_CONV_STACK, 0)
+    assert np.array_equal(got, conv_ref(x, w))
 
 
 def test_integer_inputs_fp16_are_exact(lib):
@@ -129,8 +154,19 @@ def test_argument_errors_are_reported(lib):
     assert run(h, x.data_ptr(), 16, ins, x.data_ptr(), 16, ks, y.data_ptr(), g.GEMM_F32) == g.GEMM_ERR_INVALID_ARG
     assert run(h, x.data_ptr(), 16, ins, x.data_ptr(), 16, [1, 1, 5, 2], y.data_ptr(),
                g.GEMM_BF16) == g.GEMM_ERR_INVALID_ARG
-    assert run(h, x.data_ptr(), 16, [2, 2, 4, 300], x.data_ptr(), 16, ks, y.data_ptr(),
+    # one filter triple's weights do not fit three pipeline stages
+    assert run(h, x.data_ptr(), 512, [2, 2, 4, 8], x.data_ptr(), 128, [1, 1, 1, 4], y.data_ptr(),
                g.GEMM_BF16) == g.GEMM_ERR_UNSUPPORTED
+    # a stack that does not divide in[3], or makes N = S C_out wider than 256
+    lib.set_option(g.GEMM_OPT_CONV_STACK, 4)
+    try:
+        assert run(h, x.data_ptr(), 16, [2, 2, 4, 6], x.data_ptr(), 16, ks, y.data_ptr(),
+                   g.GEMM_BF16) == g.GEMM_ERR_UNSUPPORTED
+        assert run(h, x.data_ptr(), 16, ins, x.data_ptr(), 128, ks, y.data_ptr(),
+                   g.GEMM_BF16) == g.GEMM_ERR_UNSUPPORTED
+    finally:
+        lib.set_option(g.GEMM_OPT_CONV_STACK, 0)
+    assert g.gemm_set_option(h, g.GEMM_OPT_CONV_STACK, 3) == g.GEMM_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert lib.device_status() == g.GEMM_OK
 
