@@ -395,6 +395,16 @@ def measure_extras(lib, dev, stream, peaks, fp32_peak, reps=20):
     res["conv4d_implicit"] = {"ms": round(ms_imp, 4), "tflops": round(w.flops / ms_imp / 1e9, 2),
                               "fp32_frac": round(w.flops / ms_imp / 1e9 / fp32_peak, 4), "bound": "alu",
                               "vs_im2col_plus_gemm": round((ms_col + ms) / ms_imp, 2)}
+    # the same convolution on the tensor cores: the same values rounded to bf16, channel-last
+    # (staging kernel + tcgen05 kernel, both inside the timed call)
+    xc, wc = si.channel_last(x, wt, "bf16")
+    xcd, wcd = xc.to(dev), wc.to(dev)
+    outs = [i - k + 1 for i, k in zip(c["ins"], c["ks"])]
+    ycl = torch.empty(outs + [c["cout"]], device=dev)
+    ms_tc = time_fn(lambda: lib.conv4d_cl(xcd, wcd, out=ycl))
+    res["conv4d_tc_bf16"] = {"ms": round(ms_tc, 4), "tflops": round(w.flops / ms_tc / 1e9, 2),
+                             "tensor_frac": round(w.flops / ms_tc / 1e9 / peaks["bf16_tflops"], 4), "bound": "tensor",
+                             "layout": "channel-last bf16 in, fp32 out", "vs_fp32_implicit": round(ms_imp / ms_tc, 2)}
     return res
 
 
