@@ -180,7 +180,7 @@ def kernel_source_hash(files):
 
 # the translation units whose device code a capture measured (a change there makes the
 # recorded DRAM traffic stale)
-KERNEL_SOURCES = {"tc_gemm": ["tc_gemm.cu"], "ffma_tiled": ["ffma.cu"], "skinny": ["skinny_tma.cu", "ffma.cu"],
+KERNEL_SOURCES = {"tc_gemm": ["tc_gemm.cu", "ptx.h"], "ffma_tiled": ["ffma.cu"], "skinny": ["skinny_tma.cu", "ptx.h"],
                   "im2col4d": ["im2col.cu"], "conv_implicit": ["conv_implicit.cu", "ffma.cu"]}
 
 
