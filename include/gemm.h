@@ -115,6 +115,28 @@ int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                   const void* A, int64_t lda, const void* B, int64_t ldb,
                   float* C, int64_t ldc, gemm_dtype_t dtype, void* stream);
 
+/* One product of gemm_run_host_batch: the arguments of gemm_run_host. */
+typedef struct gemm_host_problem {
+    int64_t M, N, K;
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    float* C;
+    int64_t ldc;
+    int dtype; /* gemm_dtype_t of A and B */
+} gemm_host_problem;
+
+/* Several host-memory products as one pipeline: each is staged in its own region of the
+ * handle's device buffer and split into row chunks as in gemm_run_host.  The chunks run
+ * on `stream` with half of the compute-bound products' chunks first, the transfer-bound
+ * products' chunks next and the rest last (chunks of one product in order), so copies in
+ * both directions hide under compute.  Each C is the same as gemm_run_host's.
+ * Every problem is checked before anything is queued (the first failing check is
+ * returned and nothing runs).  Returns after `stream` has been synchronised.
+ * count == 0 is a no-op. */
+int gemm_run_host_batch(gemm_handle_t h, int count, const gemm_host_problem* problems, void* stream);
+
 /* Lowering of a valid (no padding, stride 1, dilation 1) 4-D cross-correlation to a
  * GEMM operand, as in "Three X: large convolutions in PyTorch for training", section
  * "CuBLAS" (im2col / vol2col, extended by one spatial dimension):

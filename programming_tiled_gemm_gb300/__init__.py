@@ -25,10 +25,18 @@ GEMM_OPT_TEST_STALL = 6
 GEMM_OPT_CONV_STACK = 7
 
 # Every symbol include/gemm.h declares (the ABI test checks the library exports them).
-EXPORTS = ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host", "conv4d_im2col",
+EXPORTS = ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host", "gemm_run_host_batch",
+           "conv4d_im2col",
            "conv4d_forward", "conv4d_forward_cl",
            "gemm_get_device_status", "gemm_set_option", "gemm_launch_count", "gemm_status_string",
            "gemm_run_f32_skinny_noalloc"]
+
+
+class HostProblem(ctypes.Structure):
+    """gemm_host_problem: one product of gemm_run_host_batch."""
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("A", ctypes.c_void_p),
+                ("lda", ctypes.c_int64), ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64), ("C", ctypes.c_void_p),
+                ("ldc", ctypes.c_int64), ("dtype", ctypes.c_int)]
 
 
 class GemmError(RuntimeError):
@@ -46,6 +54,7 @@ def _load():
     lib.gemm_destroy.argtypes = [p]
     lib.gemm_run.argtypes = [p, i64, i64, i64, p, i64, p, i64, p, i64, i32, p]
     lib.gemm_run_host.argtypes = [p, i64, i64, i64, p, i64, p, i64, p, i64, i32, p]
+    lib.gemm_run_host_batch.argtypes = [p, i32, ctypes.POINTER(HostProblem), p]
     f32 = ctypes.c_float
     lib.gemm_run_ex.argtypes = [p, i64, i64, i64, f32, p, i64, p, i64, f32, p, i64, i32, i32, p]
     lib.conv4d_im2col.argtypes = [p, p, i64, ctypes.POINTER(i64), ctypes.POINTER(i64), p, p]
@@ -96,6 +105,12 @@ def gemm_run_ex(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ab_dtype, c_dty
 
 def gemm_run_host(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream=0) -> int:
     return _lib.gemm_run_host(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream)
+
+
+def gemm_run_host_batch(h, problems, stream=0) -> int:
+    """problems: a sequence of HostProblem (or tuples of its fields)."""
+    arr = (HostProblem * len(problems))(*[q if isinstance(q, HostProblem) else HostProblem(*q) for q in problems])
+    return _lib.gemm_run_host_batch(h, len(problems), arr, stream)
 
 
 def conv4d_im2col(h, x, C_in, in_dims, k_dims, col, stream=0) -> int:
@@ -222,6 +237,24 @@ class Gemm:
             raise GemmError(rc, "gemm_run_host")
         return out
 
+    def matmul_host_batch(self, pairs, outs=None, stream=None):
+        """Several products of CPU tensors as one pipeline: pairs = [(A, B), ...]."""
+        import torch
+        if outs is None:
+            outs = [torch.empty((A.shape[0], B.shape[1]), dtype=torch.float32) for A, B in pairs]
+        probs = []
+        for (A, B), out in zip(pairs, outs):
+            if A.shape[1] != B.shape[0] or tuple(out.shape) != (A.shape[0], B.shape[1]) or A.dtype != B.dtype:
+                raise ValueError("shapes or dtypes do not match")
+            probs.append(HostProblem(A.shape[0], B.shape[1], A.shape[1], A.data_ptr(), _row_major_2d(A, "A"),
+                                     B.data_ptr(), _row_major_2d(B, "B"), out.data_ptr(), _row_major_2d(out, "out"),
+                                     _dtype_code(A)))
+        s = 0 if stream is None else int(stream)
+        rc = gemm_run_host_batch(self.handle, probs, s)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "gemm_run_host_batch")
+        return outs
+
     def im2col4d(self, x, ks, col=None, stream=None):
         """Column matrix [C_in*prod(ks), prod(in-ks+1)] of a valid 4-D cross-correlation."""
         import torch
@@ -303,7 +336,8 @@ class Gemm:
         return gemm_get_device_status(self.handle, s)
 
 
-__all__ = ["Gemm", "GemmError", "gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host",
+__all__ = ["Gemm", "GemmError", "HostProblem", "gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex",
+           "gemm_run_host", "gemm_run_host_batch",
            "conv4d_im2col", "conv4d_forward", "conv4d_forward_cl", "gemm_get_device_status", "gemm_set_option", "gemm_launch_count",
            "gemm_status_string",
            "status_string", "library", "LIB_PATH", "EXPORTS"]

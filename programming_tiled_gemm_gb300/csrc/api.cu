@@ -10,6 +10,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "internal.h"
 
@@ -21,10 +22,10 @@ struct gemm_ctx {
     int* d_status = nullptr;  // device status word written by kernels with bounded waits
     float* workspace = nullptr;
     size_t workspace_bytes = 0;
-    void* stage[3] = {nullptr, nullptr, nullptr};  // gemm_run_host device copies of A, B, C
+    void* host_stage = nullptr;  // gemm_run_host(_batch) device copies of A, B and C
+    size_t host_stage_bytes = 0;
     float* product = nullptr;  // fp32 product for the generalised epilogue of fp32 inputs
     size_t product_bytes = 0;
-    size_t stage_bytes[3] = {0, 0, 0};
     int opt_f32_kernel = 0;
     int opt_split_k = 0;
     int opt_tc_chunk = 0;  // tensor-core accumulation chunk in 64-wide k-blocks (0 = default)
@@ -183,8 +184,7 @@ int gemm_destroy(gemm_handle_t h)
     if (h->d_status) cudaFree(h->d_status);
     if (h->workspace) cudaFree(h->workspace);
     if (h->product) cudaFree(h->product);
-    for (int i = 0; i < 3; ++i)
-        if (h->stage[i]) cudaFree(h->stage[i]);
+    if (h->host_stage) cudaFree(h->host_stage);
     delete h;
     return GEMM_OK;
 }
@@ -312,72 +312,168 @@ int ensure_pipeline(gemm_handle_t h)
     return GEMM_OK;
 }
 
+// Device staging of one host problem: A, B and C with leading dimensions rounded up to
+// multiples of 8 (16-bit) / 4 (fp32) elements, so every row is 16-byte aligned.
+struct HostStage {
+    int64_t lda_d, ldb_d, ldc_d;
+    size_t a_off, b_off, c_off, bytes;  // offsets in the handle's staging buffer
+};
+
+HostStage host_stage_layout(const gemm_host_problem& q, size_t base)
+{
+    const size_t es = (q.dtype == GEMM_F32) ? 4 : 2;
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    HostStage st;
+    st.lda_d = (q.K + 7) / 8 * 8;
+    st.ldb_d = (q.N + 7) / 8 * 8;
+    st.ldc_d = (q.N + 3) / 4 * 4;
+    st.a_off = base;
+    st.b_off = st.a_off + up(q.K > 0 ? (size_t)q.M * st.lda_d * es : 0);
+    st.c_off = st.b_off + up(q.K > 0 ? (size_t)q.K * st.ldb_d * es : 0);
+    st.bytes = st.c_off + up((size_t)q.M * st.ldc_d * 4) - base;
+    return st;
+}
+
+// Row chunks of one host problem: 16-bit inputs are transfer-bound (the tensor cores
+// outrun a ~200 GB/s host link), so they take up to 8 chunks of >= 1024 rows; fp32 is
+// compute-bound, so 2 chunks of >= 2048 rows keep its launches full.
+void host_chunks(const gemm_host_problem& q, int64_t* chunk, int* nchunks)
+{
+    *chunk = q.M;
+    *nchunks = (q.M > 0 && q.N > 0) ? 1 : 0;
+    const int64_t min_rows = (q.dtype == GEMM_F32) ? 2048 : 1024;
+    const int max_chunks = (q.dtype == GEMM_F32) ? 2 : gemm_ctx::kMaxChunks;
+    if (q.K > 0 && q.N > 0 && q.M >= 2 * min_rows) {
+        int n = (int)(q.M / min_rows);
+        if (n > max_chunks) n = max_chunks;
+        *chunk = ((q.M + n - 1) / n + 255) / 256 * 256;
+        *nchunks = (int)((q.M + *chunk - 1) / *chunk);
+    }
+}
+
+// A problem whose estimated compute time exceeds its estimated transfer time (rates of
+// this GPU's tensor / FP32 pipes and host link, for ordering only).
+bool compute_bound(const gemm_host_problem& q)
+{
+    const double flops = 2.0 * (double)q.M * (double)q.N * (double)q.K;
+    const double es = (q.dtype == GEMM_F32) ? 4.0 : 2.0;
+    const double bytes = es * ((double)q.M * q.K + (double)q.K * q.N) + 4.0 * (double)q.M * q.N;
+    const double t_compute = flops / ((q.dtype == GEMM_F32) ? 5.5e13 : 1.5e15);
+    const double t_copy = bytes / 3.4e11;
+    return t_compute >= t_copy;
+}
+
+struct HostChunk {
+    int prob;
+    int64_t m0, rows;
+};
+
+// Enqueue one row chunk: its A rows (and, before a problem's first chunk, all of B) go in
+// on s_in, the chunk's product runs on `s` once they are in, and its C rows come back on
+// s_out while later chunks compute.  Nothing waits on the host.
+int enqueue_host_chunk(gemm_handle_t h, const gemm_host_problem& q, const HostStage& st, const HostChunk& c,
+                       bool first, int ev, cudaStream_t s)
+{
+    const size_t es = (q.dtype == GEMM_F32) ? 4 : 2;
+    uint8_t* base = static_cast<uint8_t*>(h->host_stage);
+    uint8_t* Ad = base + st.a_off;
+    uint8_t* Bd = base + st.b_off;
+    float* Cd = reinterpret_cast<float*>(base + st.c_off);
+    const uint8_t* Ah = static_cast<const uint8_t*>(q.A);
+    if (q.K > 0) {
+        if (first &&
+            copy_rows(Bd, st.ldb_d * es, q.B, q.ldb * es, q.N * es, q.K, cudaMemcpyHostToDevice, h->s_in) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (copy_rows(Ad + c.m0 * st.lda_d * es, st.lda_d * es, Ah + c.m0 * q.lda * es, q.lda * es, q.K * es, c.rows,
+                      cudaMemcpyHostToDevice, h->s_in) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    if (cudaEventRecord(h->ev_a[ev], h->s_in) != cudaSuccess || cudaStreamWaitEvent(s, h->ev_a[ev], 0) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    const int rc = gemm_run(h, c.rows, q.N, q.K, Ad + c.m0 * st.lda_d * es, st.lda_d, Bd, st.ldb_d,
+                            Cd + c.m0 * st.ldc_d, st.ldc_d, (gemm_dtype_t)q.dtype, s);
+    if (rc != GEMM_OK) return rc;
+    if (cudaEventRecord(h->ev_c[ev], s) != cudaSuccess || cudaStreamWaitEvent(h->s_out, h->ev_c[ev], 0) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (copy_rows(q.C + c.m0 * q.ldc, q.ldc * 4, Cd + c.m0 * st.ldc_d, st.ldc_d * 4, q.N * 4, c.rows,
+                  cudaMemcpyDeviceToHost, h->s_out) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+// Run `count` host problems as one pipeline and wait for it.
+int run_host_problems(gemm_handle_t h, int count, const gemm_host_problem* q, void* stream)
+{
+    for (int i = 0; i < count; ++i) {
+        const int rc = check_common(h, q[i].M, q[i].N, q[i].K, q[i].A, q[i].lda, q[i].B, q[i].ldb, q[i].C, q[i].ldc,
+                                    q[i].dtype);
+        if (rc != GEMM_OK) return rc;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DeviceGuard g(h->device);
+    if (!g.ok()) return GEMM_ERR_CUDA;
+    // every problem stages in its own region, so later problems' inputs travel while
+    // earlier ones compute and drain
+    size_t total = 0;
+    for (int i = 0; i < count; ++i) total += host_stage_layout(q[i], total).bytes;
+    int rc = ensure_buffer(&h->host_stage, &h->host_stage_bytes, total);
+    if (rc != GEMM_OK) return rc;
+    if ((rc = ensure_pipeline(h)) != GEMM_OK) return rc;
+    if (cudaEventRecord(h->ev_start, s) != cudaSuccess || cudaStreamWaitEvent(h->s_in, h->ev_start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(h->s_out, h->ev_start, 0) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    std::vector<HostStage> st(count);
+    size_t off = 0;
+    for (int i = 0; i < count; ++i) {
+        st[i] = host_stage_layout(q[i], off);
+        off += st[i].bytes;
+    }
+    // Chunk order on the compute stream: half of the compute-bound problems' chunks, then
+    // the transfer-bound problems' chunks, then the rest.  The first compute starts after
+    // a short upload, the transfer-bound chunks' copies hide under compute on both sides,
+    // and the last chunk's result is short to bring back.  Chunks of one problem keep
+    // their order (its B goes in before its first chunk).
+    std::vector<HostChunk> cb, tb;
+    for (int i = 0; i < count; ++i) {
+        int64_t chunk;
+        int n;
+        host_chunks(q[i], &chunk, &n);
+        for (int c = 0; c < n; ++c) {
+            const int64_t m0 = c * chunk, rows = (q[i].M - m0) < chunk ? (q[i].M - m0) : chunk;
+            (compute_bound(q[i]) ? cb : tb).push_back({i, m0, rows});
+        }
+    }
+    std::vector<HostChunk> order(cb.begin(), cb.begin() + (cb.size() + 1) / 2);
+    order.insert(order.end(), tb.begin(), tb.end());
+    order.insert(order.end(), cb.begin() + (cb.size() + 1) / 2, cb.end());
+    std::vector<char> started(count, 0);
+    for (size_t k = 0; k < order.size(); ++k) {
+        const HostChunk& c = order[k];
+        // an event pair is recorded, waited on, then reused: each wait takes the record
+        // that precedes it
+        rc = enqueue_host_chunk(h, q[c.prob], st[c.prob], c, !started[c.prob], (int)(k % gemm_ctx::kMaxChunks), s);
+        if (rc != GEMM_OK) return rc;
+        started[c.prob] = 1;
+    }
+    if (cudaEventRecord(h->ev_done, h->s_out) != cudaSuccess || cudaStreamWaitEvent(s, h->ev_done, 0) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return from_cuda(cudaStreamSynchronize(s));
+}
+
 }  // namespace
 
 extern "C" int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                              const void* B, int64_t ldb, float* C, int64_t ldc, gemm_dtype_t dtype, void* stream)
 {
-    int rc = check_common(h, M, N, K, A, lda, B, ldb, C, ldc, (int)dtype);
-    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    DeviceGuard g(h->device);
-    if (!g.ok()) return GEMM_ERR_CUDA;
-    const size_t es = (dtype == GEMM_F32) ? 4 : 2;
-    // device leading dimensions: multiples of 8 elements keep every row 16-byte aligned
-    const int64_t lda_d = (K + 7) / 8 * 8, ldb_d = (N + 7) / 8 * 8, ldc_d = (N + 3) / 4 * 4;
-    if (K > 0) {
-        if ((rc = ensure_buffer(&h->stage[0], &h->stage_bytes[0], (size_t)M * lda_d * es)) != GEMM_OK) return rc;
-        if ((rc = ensure_buffer(&h->stage[1], &h->stage_bytes[1], (size_t)K * ldb_d * es)) != GEMM_OK) return rc;
-    }
-    if ((rc = ensure_buffer(&h->stage[2], &h->stage_bytes[2], (size_t)M * ldc_d * 4)) != GEMM_OK) return rc;
-    if ((rc = ensure_pipeline(h)) != GEMM_OK) return rc;
+    const gemm_host_problem q = {M, N, K, A, lda, B, ldb, C, ldc, (int)dtype};
+    return run_host_problems(h, 1, &q, stream);
+}
 
-    // Pipeline over row chunks of A and C: B and A chunk i go in on s_in, the product of
-    // chunk i runs on the caller's stream once its rows are in, and C chunk i comes back
-    // on s_out while later chunks still compute.  16-bit inputs are transfer-bound (the
-    // tensor cores outrun a ~200 GB/s host link), so they take up to 8 chunks of >= 1024
-    // rows; fp32 is compute-bound, so 2 chunks of >= 2048 rows keep its launches full.
-    int64_t chunk = M;
-    int nchunks = 1;
-    const int64_t min_rows = (dtype == GEMM_F32) ? 2048 : 1024;
-    const int max_chunks = (dtype == GEMM_F32) ? 2 : gemm_ctx::kMaxChunks;
-    if (K > 0 && M >= 2 * min_rows) {
-        nchunks = (int)(M / min_rows);
-        if (nchunks > max_chunks) nchunks = max_chunks;
-        chunk = ((M + nchunks - 1) / nchunks + 255) / 256 * 256;
-        nchunks = (int)((M + chunk - 1) / chunk);
-    }
-    uint8_t* Ad = static_cast<uint8_t*>(h->stage[0]);
-    float* Cd = static_cast<float*>(h->stage[2]);
-    const uint8_t* Ah = static_cast<const uint8_t*>(A);
-    float* Ch = C;
-    if (cudaEventRecord(h->ev_start, s) != cudaSuccess || cudaStreamWaitEvent(h->s_in, h->ev_start, 0) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    if (K > 0 && copy_rows(h->stage[1], ldb_d * es, B, ldb * es, N * es, K, cudaMemcpyHostToDevice, h->s_in) !=
-                     cudaSuccess)
-        return GEMM_ERR_CUDA;
-    for (int i = 0; i < nchunks; ++i) {
-        const int64_t m0 = i * chunk, rows = (M - m0) < chunk ? (M - m0) : chunk;
-        if (K > 0 && copy_rows(Ad + m0 * lda_d * es, lda_d * es, Ah + m0 * lda * es, lda * es, K * es, rows,
-                               cudaMemcpyHostToDevice, h->s_in) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        if (cudaEventRecord(h->ev_a[i], h->s_in) != cudaSuccess) return GEMM_ERR_CUDA;
-    }
-    for (int i = 0; i < nchunks; ++i) {
-        const int64_t m0 = i * chunk, rows = (M - m0) < chunk ? (M - m0) : chunk;
-        if (cudaStreamWaitEvent(s, h->ev_a[i], 0) != cudaSuccess) return GEMM_ERR_CUDA;
-        rc = gemm_run(h, rows, N, K, Ad + m0 * lda_d * es, lda_d, h->stage[1], ldb_d, Cd + m0 * ldc_d, ldc_d, dtype,
-                      stream);
-        if (rc != GEMM_OK) return rc;
-        if (cudaEventRecord(h->ev_c[i], s) != cudaSuccess || cudaStreamWaitEvent(h->s_out, h->ev_c[i], 0) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        if (copy_rows(Ch + m0 * ldc, ldc * 4, Cd + m0 * ldc_d, ldc_d * 4, N * 4, rows, cudaMemcpyDeviceToHost,
-                      h->s_out) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-    }
-    if (cudaEventRecord(h->ev_done, h->s_out) != cudaSuccess || cudaStreamWaitEvent(s, h->ev_done, 0) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    return from_cuda(cudaStreamSynchronize(s));
+extern "C" int gemm_run_host_batch(gemm_handle_t h, int count, const gemm_host_problem* problems, void* stream)
+{
+    if (!h || count < 0 || (count > 0 && !problems)) return GEMM_ERR_INVALID_ARG;
+    if (count == 0) return GEMM_OK;
+    return run_host_problems(h, count, problems, stream);
 }
 
 extern "C" {

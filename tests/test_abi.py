@@ -68,6 +68,9 @@ def test_null_handle_is_rejected_without_touching_cuda(pkg):
     ins = (ctypes.c_int64 * 4)(4, 4, 4, 4)
     assert lib.conv4d_im2col(None, 1, 1, ins, ins, 1, None) == pkg.GEMM_ERR_INVALID_ARG
     assert lib.conv4d_forward(None, 1, 1, ins, 1, 1, ins, 1, 1, None) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.conv4d_forward_cl(None, 1, 16, ins, 1, 16, ins, 1, pkg.GEMM_BF16, None) == pkg.GEMM_ERR_INVALID_ARG
+    probs = (pkg.HostProblem * 1)(pkg.HostProblem(4, 4, 4, 1, 4, 1, 4, 1, 4, 0))
+    assert lib.gemm_run_host_batch(None, 1, probs, None) == pkg.GEMM_ERR_INVALID_ARG
 
 
 def test_create_without_a_gpu_reports_an_error(pkg):

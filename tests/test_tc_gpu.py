@@ -197,3 +197,33 @@ def test_host_entry_point_pipelined_chunks(lib, pinned, dtype):
     ref = oracle.gemm(A.float().numpy(), B.float().numpy())
     assert np.array_equal(Cbig[:, :N].double().numpy(), ref)
     assert torch.all(Cbig[:, N:] == -3.0)
+
+
+def test_host_batch_pipelines_several_products(lib):
+    """gemm_run_host_batch: a chunked bf16 product, an fp32 product, an fp16 product with
+    padded host leading dimensions and an empty one, in one pipeline; integer inputs: exact,
+    and each result equals the single-product entry point's."""
+    import programming_tiled_gemm_gb300 as g
+    shapes = [(4352 + 3, 264, 72, "bf16"), (4100, 136, 40, "f32"), (300, 72, 520, "f16"), (0, 8, 8, "bf16")]
+    pairs, outs, refs = [], [], []
+    for i, (M, N, K, dt) in enumerate(shapes):
+        A, B = si.integer_copy(M, N, K, seed=60 + i, dtype=dt)
+        Abig = torch.zeros((M, K + 8), dtype=A.dtype).pin_memory()
+        Abig[:, :K] = A
+        Cbig = torch.full((M, N + 4), -3.0).pin_memory()
+        pairs.append((Abig[:, :K], B.pin_memory()))
+        outs.append(Cbig)
+        refs.append(oracle.gemm(A.float().numpy(), B.float().numpy()))
+    lib.matmul_host_batch(pairs, outs=[c[:, :N] for c, (_, N, _, _) in zip(outs, shapes)])
+    for (M, N, K, dt), Cbig, ref, (A, B) in zip(shapes, outs, refs, pairs):
+        assert np.array_equal(Cbig[:, :N].double().numpy(), ref)
+        assert torch.all(Cbig[:, N:] == -3.0)
+        if M:
+            assert torch.equal(lib.matmul_host(A, B), Cbig[:, :N])
+    # a bad problem anywhere in the batch: nothing runs
+    C0 = torch.full((4, 4), 5.0)
+    bad = [g.HostProblem(4, 4, 4, pairs[0][0].data_ptr(), 80, pairs[0][1].data_ptr(), 264, C0.data_ptr(), 4,
+                         g.GEMM_BF16),
+           g.HostProblem(4, 4, 4, 0, 4, 0, 4, C0.data_ptr(), 4, g.GEMM_BF16)]
+    assert g.gemm_run_host_batch(lib.handle, bad) == g.GEMM_ERR_INVALID_ARG
+    assert torch.all(C0 == 5.0)
