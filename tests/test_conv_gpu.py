@@ -33,6 +33,8 @@ SHAPES = [
     (3, (6, 7, 5, 9), 4, (2, 3, 1, 4)),   # column count 5*5*5*6 = 750: not a multiple of 4
     (4, (8, 8, 8, 8), 32, (3, 3, 3, 3)),
     (16, (9, 9, 9, 9), 32, (5, 5, 5, 5)),
+    (3, (6, 5, 7, 12), 4, (2, 1, 3, 5)),  # five-tap rows, p3 = 8: the tap-group im2col path
+    (2, (4, 5, 6, 16), 3, (2, 3, 2, 5)),  # the same with p3 = 12, as in the 16^4 workload
 ]
 
 
