@@ -26,11 +26,14 @@
 //     tile's last chunk is in.  While it works on one chunk, the MMA fills the other
 //     buffer, so the epilogue is hidden behind the main loop.
 // Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
-// warps 2..9 = epilogue (two warps per 32-lane TMEM quarter, 128 columns each).  A
-// 4-stage ring of shared-memory buffers links producer and MMA through mbarriers.  The grid is persistent (one CTA per SM) and walks output tiles in
-// groups of 16 tile-rows so that concurrently running tiles share A rows and B columns
-// in L2 ("CUDA overview: performance surprises", section "Parallelism first": enough
-// independent work per SM, no idle units).
+// warps 2..9 = epilogue (two warps per 32-lane TMEM quarter, 128 columns each).  A ring
+// of shared-memory stages (4 for single CTAs, 6 for CTA pairs) links producer and MMA
+// through mbarriers.  The grid is persistent (one CTA, or CTA pair, per SM or SM pair)
+// and walks output tiles in groups of tile-rows (16 rows of 128 for single CTAs, 2048 rows
+// for pairs) so that concurrently running tiles share A rows and B columns in L2 ("CUDA
+// overview: performance surprises", section "Parallelism first": enough independent work
+// per SM, no idle units).  The CTA-pair kernel below (cta_group::2) is the default for
+// M > 128.
 //
 // Every wait on an mbarrier is bounded (a wall-clock limit read from %globaltimer).  On
 // expiry the thread records an error code in the caller-visible status word, the CTA
