@@ -205,7 +205,10 @@ typedef enum {
     GEMM_OPT_TC_CHUNK = 4,      /* 0 default (16), else the tensor-core accumulation chunk in 64-wide k-blocks
                                    (1..4096): the tensor core's fp32 accumulator is restarted every chunk and
                                    chunk sums are added in fp32 round-to-nearest */
-    GEMM_OPT_TC_PAIR = 5,       /* tensor-core tiles: 0 choose (default: pairs when M > 128), 1 one CTA per
+    GEMM_OPT_TC_PAIR = 5,       /* tensor-core tiles: 0 choose (default: pairs when M > 128; for M <= 128 with
+                                   128x256 tiles that fill under half the SMs, K split into 2 to 16 slices,
+                                   one CTA each, on a cluster per tile that adds the fp32 partial tiles in
+                                   slice order through distributed shared memory), 1 one CTA per
                                    128x256 tile, 2 a pair of CTAs (cluster of two) per 256x256 tile, 3 two
                                    pairs (cluster of four) per 512x256 tile, B read once for both pairs */
     GEMM_OPT_TEST_STALL = 6,    /* test hook for failure detection, 0 (default) or 1: the kernels with

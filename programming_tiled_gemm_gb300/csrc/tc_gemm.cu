@@ -44,6 +44,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -68,6 +69,14 @@ constexpr int B_STAGE_BYTES = BN * BK * 2;   // 32 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;            // two chunk accumulators
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
+// Split-K: a slice's fp32 partial tile, kept in its CTA's shared memory (the operand ring,
+// free once the tile's MMAs are done) as BM rows of BN * 4 bytes; 16-byte chunk c of row r
+// sits at chunk c ^ (r & 7), so that the epilogue's row-per-thread stores and the
+// reduction's row-contiguous loads are both free of bank conflicts.
+constexpr int SPLIT_ROW_BYTES = BN * 4;
+constexpr int MAX_SPLIT = 16;  // K slices per tile (cluster size; above 8 is non-portable)
+static_assert(BM * SPLIT_ROW_BYTES <= STAGES * STAGE_BYTES, "partial tile must fit the operand ring");
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A K-major, B N-major (B is the
 // row-major K x N operand), N = 256; M = 128 for one CTA, 256 for a CTA pair.
@@ -102,7 +111,10 @@ struct TcParams {
     int64_t ldc;
     int m_blocks, n_blocks, num_tiles, k_blocks;
     int kc;       // k-blocks per accumulation chunk
-    int nchunks;  // chunks per tile
+    int nchunks;  // chunks per tile (per K slice with split-K)
+    int nsplit;   // single-CTA kernel: K slices of a tile, one CTA each, as one cluster
+                  // (work item = tile * nsplit + slice); 1 = no split.  Slice z covers
+                  // k-blocks [z * k_blocks / nsplit, (z + 1) * k_blocks / nsplit)
     int group_m;  // tile rows per raster group
     uint32_t idesc;
     int vec_store;
@@ -179,10 +191,63 @@ __device__ __forceinline__ void epi_store4(const TcParams& p, int64_t off, int n
     }
 }
 
+__device__ __forceinline__ int slice_begin(const TcParams& p, int z)
+{
+    return (int)((int64_t)z * p.k_blocks / p.nsplit);
+}
+
 __device__ __forceinline__ void record_error(int* status, int code, volatile int* abort_flag)
 {
     atomicCAS(status, 0, code);
     *abort_flag = 1;
+}
+
+// Split-K output: this CTA (rank r of the tile's cluster of S slices) adds, for its share
+// of the tile's 16-byte chunks, the S partial tiles in slice order (read from each CTA's
+// shared memory) and stores C.  e = 0 .. EPI_THREADS - 1.
+__device__ __forceinline__ void split_reduce_store(const TcParams& p, uint32_t part, int tile, int e)
+{
+    constexpr int CHUNKS = BM * BN / 4;
+    const int S = p.nsplit;
+    const int r = (int)cluster_ctarank();
+    const TileCoord tc = tile_coord(tile, p.m_blocks, p.n_blocks);
+    const int lo = (int)((int64_t)CHUNKS * r / S), hi = (int)((int64_t)CHUNKS * (r + 1) / S);
+    uint32_t peer[MAX_SPLIT];
+#pragma unroll
+    for (int z = 0; z < MAX_SPLIT; ++z)
+        if (z < S) peer[z] = mapa_shared(part, (uint32_t)z);
+#pragma unroll 2
+    for (int idx = lo + e; idx < hi; idx += EPI_THREADS) {
+        const int rr = idx / (BN / 4), c = idx % (BN / 4);
+        const uint32_t off = (uint32_t)(rr * SPLIT_ROW_BYTES + ((c ^ (rr & 7)) << 4));
+        float4 v[MAX_SPLIT];
+#pragma unroll
+        for (int z = 0; z < MAX_SPLIT; ++z)
+            if (z < S) v[z] = ld_shared_cluster_f4(peer[z] + off);
+        float4 acc = v[0];
+#pragma unroll
+        for (int z = 1; z < MAX_SPLIT; ++z)
+            if (z < S) {
+                acc.x = __fadd_rn(acc.x, v[z].x), acc.y = __fadd_rn(acc.y, v[z].y);
+                acc.z = __fadd_rn(acc.z, v[z].z), acc.w = __fadd_rn(acc.w, v[z].w);
+            }
+        const int row = tc.m_blk * BM + rr, col = tc.n_blk * BN + 4 * c;
+        if (row >= p.M || col >= p.N) continue;
+        const bool full = p.vec_store && col + 4 <= p.N;
+        if (!p.epi_plain) {
+            epi_store4(p, (int64_t)row * p.ldc + col, p.N - col, acc.x, acc.y, acc.z, acc.w, full);
+        } else {
+            float* cp = static_cast<float*>(p.C) + (int64_t)row * p.ldc + col;
+            if (full) {
+                *reinterpret_cast<float4*>(cp) = acc;
+            } else {
+                const float w[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (col + j < p.N) cp[j] = w[j];
+            }
+        }
+    }
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -238,9 +303,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t phase = 0;
             uint32_t issued_mask = 0, last_parity = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+            for (int it = blockIdx.x; it < p.num_tiles * p.nsplit && ok; it += gridDim.x) {
+                const int t = it / p.nsplit, sl = it % p.nsplit;
                 const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                const int kb_end = slice_begin(p, sl + 1);
+                for (int kb = slice_begin(p, sl); kb < kb_end; ++kb) {
                     if (*abort_flag || !mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.limit_ns)) {
                         record_error(p.status, kDevTimeoutProducer, abort_flag);
                         ok = false;
@@ -277,8 +344,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t buf_phase = 0;
             bool ok = true;
             const uint32_t a_base = smem_u32(smem_a), b_base = smem_u32(smem_b);
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+            for (int it = blockIdx.x; it < p.num_tiles * p.nsplit && ok; it += gridDim.x) {
+                const int sl = it % p.nsplit;
+                const int kb_beg = slice_begin(p, sl), kb_end = slice_begin(p, sl + 1);
                 for (int ch = 0; ch < p.nchunks && ok; ++ch) {
+                    const int kb0 = kb_beg + ch * p.kc;
+                    if (kb0 >= kb_end) break;  // a short last slice has fewer chunks
                     if (*abort_flag || !mbar_wait(smem_u32(&tempty_bar[buf]), buf_phase ^ 1, p.limit_ns)) {
                         record_error(p.status, kDevTimeoutMma, abort_flag);
                         ok = false;
@@ -286,8 +357,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-                    const int kb0 = ch * p.kc;
-                    const int kb1 = min(kb0 + p.kc, p.k_blocks);
+                    const int kb1 = min(kb0 + p.kc, kb_end);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (*abort_flag || !mbar_wait(smem_u32(&full_bar[stage]), phase, p.limit_ns)) {
                             record_error(p.status, kDevTimeoutMma, abort_flag);
@@ -339,11 +409,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             bool ok = mbar_wait(smem_u32(never_bar), 0, p.limit_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok && lane == 0) record_error(p.status, kDevTimeoutEpilogue, abort_flag);
-            t_first = p.num_tiles;
+            t_first = p.num_tiles * p.nsplit;
         }
-        for (int t = t_first; t < p.num_tiles; t += gridDim.x) {
+        for (int it = t_first; it < p.num_tiles * p.nsplit; it += gridDim.x) {
+            const int t = it / p.nsplit, sl = it % p.nsplit;
+            const int kb_beg = slice_begin(p, sl), kb_end = slice_begin(p, sl + 1);
             bool ok = true;
+#pragma unroll
+            for (int i = 0; i < EPI_COLS; ++i) tot[i] = 0.f;  // (no value lives on from the last tile)
             for (int ch = 0; ch < p.nchunks; ++ch) {
+                if (kb_beg + ch * p.kc >= kb_end) break;  // as the MMA issuer
                 ok = !*abort_flag && mbar_wait(smem_u32(&tfull_bar[buf]), buf_phase, p.limit_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
@@ -377,6 +452,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!ok) break;
             const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks);
             const int row = tc.m_blk * BM + q * 32 + lane;
+            if (p.nsplit > 1) {
+                // K-sliced tile (this CTA's only one): the partial product goes to this
+                // CTA's shared memory; the cluster adds the slices after the loop
+                const int rr = q * 32 + lane;
+                uint8_t* prow = smem + rr * SPLIT_ROW_BYTES;
+#pragma unroll
+                for (int j = 0; j < EPI_COLS / 4; ++j) {
+                    const int c = half * (EPI_COLS / 4) + j;
+                    *reinterpret_cast<float4*>(prow + ((c ^ (rr & 7)) << 4)) =
+                        make_float4(tot[4 * j], tot[4 * j + 1], tot[4 * j + 2], tot[4 * j + 3]);
+                }
+                continue;
+            }
             if (row < p.M && !p.epi_plain) {
                 const int col0 = tc.n_blk * BN + half * EPI_COLS;
                 const bool full = p.vec_store && col0 + EPI_COLS <= p.N;
@@ -402,6 +490,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
     }
 
+    if (p.nsplit > 1) {
+        // Every thread of every CTA of the cluster passes both barriers, on every path:
+        // the first publishes all slices' partial tiles, the second keeps each CTA's
+        // shared memory alive until the others have read it.
+        __syncwarp();
+        cluster_sync_all();
+        if (warp >= 2) split_reduce_store(p, smem_u32(smem), (int)(blockIdx.x / p.nsplit), threadIdx.x - 64);
+        __syncwarp();
+        cluster_sync_all();
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -427,21 +525,6 @@ constexpr int P_A_STAGE_BYTES = BM * BK * 2;                     // 16 KiB: this
 constexpr int P_B_STAGE_BYTES = (BN / 2) * BK * 2;               // 16 KiB: this CTA's 128 columns of B
 constexpr int P_STAGE_BYTES = P_A_STAGE_BYTES + P_B_STAGE_BYTES; // per CTA
 constexpr int p_smem_bytes(int stages) { return stages * P_STAGE_BYTES + 1024 + 1024; }
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Address of the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
@@ -471,11 +554,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
         if (mbar_try_wait_cluster(bar, parity)) return true;
         if ((abort_flag && *abort_flag) || global_timer() - t0 > limit_ns) return false;
     }
-}
-
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
@@ -838,6 +916,53 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
+namespace {
+
+// Clusters of `S` single-CTA kernels that can be resident at once (0: none), per size.
+int split_clusters_fit(int S)
+{
+    static std::atomic<int> cache[MAX_SPLIT + 1];
+    static std::once_flag once;
+    std::call_once(once, [] {
+        for (auto& c : cache) c.store(-1);
+    });
+    int v = cache[S].load();
+    if (v >= 0) return v;
+    v = 0;
+    if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(S, 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = S;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&v, tc_gemm_kernel, &cfg) != cudaSuccess) v = 0;
+    }
+    cudaGetLastError();  // a refused size leaves no sticky error behind
+    cache[S].store(v);
+    return v;
+}
+
+// K slices for an M <= 128 product whose 128 x 256 tiles fill under half the SMs: the
+// largest power of two that keeps every slice at least 4 k-blocks deep, the grid within
+// the SMs and every tile's cluster resident at once.  1 = no split.
+int choose_split(int64_t tiles, int64_t k_blocks, int num_sms)
+{
+    if (2 * tiles > num_sms) return 1;
+    for (int S = MAX_SPLIT; S >= 2; S /= 2)
+        if (k_blocks >= 4 * S && tiles * S <= num_sms && split_clusters_fit(S) >= tiles) return S;
+    return 1;
+}
+
+}  // namespace
+
 int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_limit_ns, int kc_blocks,
                    int pair_mode, cudaStream_t stream, int* launches)
 {
@@ -865,6 +990,7 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.k_blocks = (int)((a.K + BK - 1) / BK);
     p.kc = kc_blocks > 0 ? kc_blocks : 16;
     p.group_m = GROUP_M;
+    p.nsplit = 1;
     p.nchunks = (p.k_blocks + p.kc - 1) / p.kc;
     p.idesc = make_idesc(bf16);
     // vector stores: 4 outputs per access (16 bytes fp32, 8 bytes bf16/fp16)
@@ -918,6 +1044,33 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
         if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < clusters)
             cfg.gridDim = dim3(cl * fit, 1, 1);
         if (cudaLaunchKernelEx(&cfg, kern, tmA, use_quad ? tmBq : tmB, p) != cudaSuccess) return GEMM_ERR_CUDA;
+        *launches += 1;
+        return GEMM_OK;
+    }
+    // M <= 128 with few tiles (chosen tiles only; the stall hook runs unsplit): K slices
+    // of a tile on a cluster of CTAs, one slice each, added through distributed shared
+    // memory in slice order
+    const int S = (pair_mode == 0 && !a.test_stall && a.M <= BM) ? choose_split(tiles, p.k_blocks, num_sms) : 1;
+    if (S > 1) {
+        p.nsplit = S;
+        const int depth = (p.k_blocks + S - 1) / S;  // the deepest slice
+        p.nchunks = (depth + p.kc - 1) / p.kc;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(tiles * S), 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = S;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (S > 8 && cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                         cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, tc_gemm_kernel, tmA, tmB, p) != cudaSuccess) return GEMM_ERR_CUDA;
         *launches += 1;
         return GEMM_OK;
     }

@@ -119,6 +119,62 @@ def test_results_are_deterministic(lib):
         assert torch.equal(c1, c3)
 
 
+SPLIT_SHAPES = [  # M <= 128 with 128 x 256 tiles filling under half the SMs: K is split
+    (128, 2048, 4096),   # 8 tiles, up to 16 slices of 4 k-blocks (clusters above 8 CTAs)
+    (100, 1000, 4296),   # ragged M and K: slices of 4 and 5 k-blocks, a partial k-block
+    (1, 256, 1024),      # one row, one tile, 4 slices
+    (37, 4104, 8192),    # 17 tiles, a partial last tile column
+    (50, 1001, 2000),    # odd N: C stored element by element
+    (128, 8, 2048),      # one narrow tile, 8 slices
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
+def test_split_k_integer_inputs_exact(lib, dtype, M, N, K):
+    """The default tile choice splits K for small M: the CTAs of a cluster each take one K
+    slice of a tile and add the fp32 partial tiles, read from each other's shared memory,
+    in slice order."""
+    A, B = si.integer_copy(M, N, K, seed=M + 5 * N + K, dtype=dtype)
+    got = run_guarded(lib, A, B)
+    assert np.array_equal(got, oracle.gemm(A.float().numpy(), B.float().numpy()))
+
+
+def test_split_k_within_tolerance_deterministic_and_close_to_unsplit(lib):
+    import programming_tiled_gemm_gb300 as g
+    M, N, K = 128, 2048, 8192
+    A, B = si.gemm_operands(M, N, K, seed=31, dist="normal", dtype="bf16")
+    got = run_guarded(lib, A, B)
+    ref = oracle.gemm(A.float().numpy(), B.float().numpy())
+    tol = 2e-5 * math.sqrt(K)
+    assert np.abs(got - ref).max() <= tol
+    Ad, Bd = A.cuda(), B.cuda()
+    launches = lib.launch_count()
+    c1 = lib.matmul(Ad, Bd).clone()
+    assert lib.launch_count() - launches == 1  # the slices are added inside the one kernel
+    for _ in range(3):
+        assert torch.equal(c1, lib.matmul(Ad, Bd))
+    lib.set_option(g.GEMM_OPT_TC_PAIR, 1)  # explicit single-CTA tiles: no split
+    c2 = lib.matmul(Ad, Bd)
+    assert (c1 - c2).abs().max().item() <= 2 * tol
+
+
+def test_split_k_general_epilogue(lib):
+    """alpha / beta and a bf16 C through the split path, alternating shapes."""
+    dev = torch.device("cuda")
+    for M, N, K in [(96, 1024, 4096), (128, 2048, 2048), (96, 1024, 4096)]:
+        A, B = si.integer_copy(M, N, K, seed=M + N + K, dtype="bf16")
+        C0 = si.ints((M, N), si.generator(3)).to(torch.bfloat16)  # integer-valued, exact in bf16
+        C = C0.to(dev)
+        lib.matmul(A.to(dev), B.to(dev), out=C, alpha=0.5, beta=-2.0)
+        torch.cuda.synchronize()
+        assert lib.device_status() == 0
+        # the exact result (integers and halves below 2^24) rounded once to bf16
+        ref = oracle.gemm_general(0.5, A.float().numpy(), B.float().numpy(), -2.0, C0.double().numpy())
+        want = torch.from_numpy(ref).float().to(torch.bfloat16)
+        assert torch.equal(C.cpu(), want)
+
+
 def test_alignment_rules(lib):
     import programming_tiled_gemm_gb300 as g
     dev = torch.device("cuda")
