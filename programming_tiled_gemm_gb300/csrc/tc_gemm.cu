@@ -68,7 +68,10 @@ constexpr int B_BOX_BYTES = B_BOX_N * BK * 2;  // 8 KiB
 constexpr int B_STAGE_BYTES = BN * BK * 2;   // 32 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;            // two chunk accumulators
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+// TMA-store epilogue: one 32 x 32 fp32 staging block per epilogue warp, after the ring
+constexpr int EPI_STAGE_BYTES = 32 * 32 * 4;
+constexpr int EPI_STAGE_TOTAL = EPI_WARPS * EPI_STAGE_BYTES;  // 32 KiB
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_TOTAL + 1024 /*barriers*/ + 1024 /*alignment slack*/;
 constexpr int EPI_THREADS = 32 * EPI_WARPS;
 // Split-K: a slice's fp32 partial tile, kept in its CTA's shared memory (the operand ring,
 // free once the tile's MMAs are done) as BM rows of BN * 4 bytes; 16-byte chunk c of row r
@@ -124,6 +127,7 @@ struct TcParams {
     float alpha, beta;  // C = alpha * (A . B) + beta * C; C unread when beta == 0
     int c_dtype;        // GEMM_F32, GEMM_BF16 or GEMM_F16
     int epi_plain;      // alpha == 1, beta == 0, fp32: plain stores
+    int c_tma;          // plain fp32 C stored by TMA through per-warp staging (tmC valid)
 };
 
 // Four adjacent outputs of the generalised product: C = alpha * acc + beta * C, in the
@@ -191,6 +195,33 @@ __device__ __forceinline__ void epi_store4(const TcParams& p, int64_t off, int n
     }
 }
 
+// Plain fp32 C from an epilogue warp: its 32 rows (thread = row lane) x EPI_COLS columns
+// of `tot`, 32 columns at a time through a 32 x 32 staging block in the 128-byte-swizzle
+// layout of tmC's box (16-byte chunk c of row r at chunk c ^ (r & 7): the row-per-thread
+// writes meet no bank conflicts), then one TMA store of full 128-byte row segments.  The
+// TMA clips rows past M and columns past N.
+__device__ __forceinline__ void store_rows_tma(const CUtensorMap* tmC, const float (&tot)[EPI_COLS], uint8_t* stg,
+                                               int row0, int col0, int M, int N, int lane)
+{
+    if (row0 >= M) return;
+#pragma unroll
+    for (int j = 0; j < EPI_COLS / 32; ++j) {
+        if (col0 + 32 * j >= N) break;
+        if (lane == 0) bulk_wait_group_read0();  // the previous block has left the staging buffer
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_float4(tot[32 * j + 4 * c], tot[32 * j + 4 * c + 1], tot[32 * j + 4 * c + 2], tot[32 * j + 4 * c + 3]);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, smem_u32(stg), col0 + 32 * j, row0);
+            bulk_commit_group();
+        }
+    }
+}
+
 __device__ __forceinline__ int slice_begin(const TcParams& p, int z)
 {
     return (int)((int64_t)z * p.k_blocks / p.nsplit);
@@ -251,7 +282,8 @@ __device__ __forceinline__ void split_reduce_store(const TcParams& p, uint32_t p
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmC, TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
@@ -259,7 +291,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
     uint8_t* smem_a = smem;
     uint8_t* smem_b = smem + STAGES * A_STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;  // [EPI_WARPS][32 rows][128 bytes]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + EPI_STAGE_TOTAL);
     uint64_t* full_bar = bars;                    // [STAGES] TMA bytes landed
     uint64_t* empty_bar = bars + STAGES;          // [STAGES] MMAs reading the stage done
     uint64_t* tfull_bar = bars + 2 * STAGES;      // [2] chunk accumulator complete
@@ -287,6 +320,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         mbar_fence_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (p.c_tma) prefetch_tensormap(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
@@ -465,7 +499,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
                 continue;
             }
-            if (row < p.M && !p.epi_plain) {
+            if (p.c_tma) {
+                store_rows_tma(&tmC, tot, epi_stage + (warp - 2) * EPI_STAGE_BYTES, tc.m_blk * BM + q * 32,
+                               tc.n_blk * BN + half * EPI_COLS, p.M, p.N, lane);
+            } else if (row < p.M && !p.epi_plain) {
                 const int col0 = tc.n_blk * BN + half * EPI_COLS;
                 const bool full = p.vec_store && col0 + EPI_COLS <= p.N;
 #pragma unroll
@@ -488,6 +525,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
         }
+        // the TMA stores of C have landed before the CTA retires
+        if (p.c_tma && lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
 
     if (p.nsplit > 1) {
@@ -524,7 +564,7 @@ constexpr int P_STAGES_DEFAULT = 6;
 constexpr int P_A_STAGE_BYTES = BM * BK * 2;                     // 16 KiB: this CTA's 128 rows of A
 constexpr int P_B_STAGE_BYTES = (BN / 2) * BK * 2;               // 16 KiB: this CTA's 128 columns of B
 constexpr int P_STAGE_BYTES = P_A_STAGE_BYTES + P_B_STAGE_BYTES; // per CTA
-constexpr int p_smem_bytes(int stages) { return stages * P_STAGE_BYTES + 1024 + 1024; }
+constexpr int p_smem_bytes(int stages) { return stages * P_STAGE_BYTES + EPI_STAGE_TOTAL + 1024 + 1024; }
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
@@ -631,14 +671,16 @@ __device__ __forceinline__ void grace_period(uint64_t ns)
 // free only when both pairs' MMAs are done with it (two arrivals on "empty").
 template <int P_STAGES, int PAIRS>
 __global__ void __launch_bounds__(THREADS, 1)
-tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p)
+tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
     uint8_t* smem_a = smem;
     uint8_t* smem_b = smem + P_STAGES * P_A_STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    uint8_t* epi_stage = smem + P_STAGES * P_STAGE_BYTES;  // [EPI_WARPS][32 rows][128 bytes]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + EPI_STAGE_TOTAL);
     uint64_t* full_bar = bars;                       // [P_STAGES] (used in the even CTA)
     uint64_t* empty_bar = bars + P_STAGES;           // [P_STAGES] (both CTAs, multicast)
     uint64_t* tfull_bar = bars + 2 * P_STAGES;       // [2] (both CTAs, multicast)
@@ -674,6 +716,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         mbar_fence_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (p.c_tma) prefetch_tensormap(&tmC);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
@@ -843,7 +886,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks, p.group_m);
             const int row = (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM + q * 32 + lane;
-            if (row < p.M && !p.epi_plain) {
+            if (p.c_tma) {
+                store_rows_tma(&tmC, tot, epi_stage + (warp - 2) * EPI_STAGE_BYTES, (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM + q * 32,
+                               tc.n_blk * BN + half * EPI_COLS, p.M, p.N, lane);
+            } else if (row < p.M && !p.epi_plain) {
                 const int col0 = tc.n_blk * BN + half * EPI_COLS;
                 const bool full = p.vec_store && col0 + EPI_COLS <= p.N;
 #pragma unroll
@@ -866,6 +912,9 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
             }
         }
+        // the TMA stores of C have landed before the CTA retires
+        if (p.c_tma && lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
 
     // after an abort, give copies and MMAs already issued time to land before the pair's
@@ -895,6 +944,22 @@ bool encode_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uin
     CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Row-major [rows][cols] fp32 C with row stride `ld` floats, stored in 32 x 32 boxes of
+// 128-byte rows in the 128-byte-swizzle layout.
+bool encode_c_f32(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols, uint64_t ld)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1000,6 +1065,10 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.beta = a.epi.beta;
     p.c_dtype = a.epi.c_dtype;
     p.epi_plain = a.epi.plain() ? 1 : 0;
+    // plain fp32 C with 16-byte aligned rows goes out through TMA stores
+    CUtensorMap tmC = tmA;  // (unused unless c_tma)
+    p.c_tma = p.epi_plain && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0 &&
+              encode_c_f32(&tmC, a.C, (uint64_t)a.M, (uint64_t)a.N, (uint64_t)a.ldc);
     p.status = dev_status;
     p.limit_ns = wait_limit_ns;
     p.test_stall = a.test_stall;
@@ -1043,7 +1112,7 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
         int fit = 0;
         if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < clusters)
             cfg.gridDim = dim3(cl * fit, 1, 1);
-        if (cudaLaunchKernelEx(&cfg, kern, tmA, use_quad ? tmBq : tmB, p) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, kern, tmA, use_quad ? tmBq : tmB, tmC, p) != cudaSuccess) return GEMM_ERR_CUDA;
         *launches += 1;
         return GEMM_OK;
     }
@@ -1070,12 +1139,12 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
         if (S > 8 && cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
                          cudaSuccess)
             return GEMM_ERR_CUDA;
-        if (cudaLaunchKernelEx(&cfg, tc_gemm_kernel, tmA, tmB, p) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, tc_gemm_kernel, tmA, tmB, tmC, p) != cudaSuccess) return GEMM_ERR_CUDA;
         *launches += 1;
         return GEMM_OK;
     }
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-    tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, p);
+    tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
     *launches += 1;
     return GEMM_OK;
