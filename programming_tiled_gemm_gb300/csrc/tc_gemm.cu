@@ -22,9 +22,13 @@
 //     registers with ordinary round-to-nearest adds, in chunk order;
 //   * the epilogue ("Three X: large convolutions in PyTorch for training", section
 //     "CUTLASS": the step after the MMA that moves accumulators out): tcgen05.ld into
-//     registers, chunk sums in registers, then vectorised stores of fp32 C once the
-//     tile's last chunk is in.  While it works on one chunk, the MMA fills the other
-//     buffer, so the epilogue is hidden behind the main loop.
+//     registers, chunk sums in registers, then, once the tile's last chunk is in, plain
+//     fp32 C goes out 32 x 32 at a time through a swizzled shared-memory block and a TMA
+//     store (coalesced 128-byte rows, clipped at the matrix edge); alpha / beta and 16-bit
+//     C use vectorised per-thread stores.  While it works on one chunk, the MMA fills the
+//     other buffer, so the epilogue is hidden behind the main loop.
+//   * M <= 128 with few tiles: K is split over the CTAs of a cluster, which add their
+//     partial tiles through distributed shared memory (see split_reduce_store).
 // Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
 // warps 2..9 = epilogue (two warps per 32-lane TMEM quarter, 128 columns each).  A ring
 // of shared-memory stages (4 for single CTAs, 6 for CTA pairs) links producer and MMA
