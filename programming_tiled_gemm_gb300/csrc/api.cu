@@ -22,6 +22,9 @@ struct gemm_ctx {
     int* d_status = nullptr;  // device status word written by kernels with bounded waits
     float* workspace = nullptr;
     size_t workspace_bytes = 0;
+    unsigned long long* tc_counters = nullptr;  // last-wave split counters of the tensor-core GEMM
+    size_t tc_counters_bytes = 0;
+    unsigned tc_seq = 0;  // tag of the last split tensor-core launch
     void* host_stage = nullptr;  // gemm_run_host(_batch) device copies of A, B and C
     size_t host_stage_bytes = 0;
     float* product = nullptr;  // fp32 product for the generalised epilogue of fp32 inputs
@@ -183,6 +186,7 @@ int gemm_destroy(gemm_handle_t h)
     }
     if (h->d_status) cudaFree(h->d_status);
     if (h->workspace) cudaFree(h->workspace);
+    if (h->tc_counters) cudaFree(h->tc_counters);
     if (h->product) cudaFree(h->product);
     if (h->host_stage) cudaFree(h->host_stage);
     delete h;
@@ -272,6 +276,24 @@ int gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha, c
         return from_cuda(e);
     }
     TcArgs t{M, N, K, A, lda, B, ldb, C, ldc, ab_dtype == GEMM_BF16 ? 1 : 0, h->opt_test_stall, epi};
+    const TcWorkspace need = tc_workspace_need(t, h->num_sms, h->opt_tc_pair);
+    if (need.floats > 0) {
+        rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes,
+                           (size_t)need.floats * sizeof(float));
+        if (rc != GEMM_OK) return rc;
+        // arrival counters: zeroed when (re)allocated and when the launch tag wraps; a
+        // launch trusts only counts that carry its own tag
+        const size_t cbytes = (size_t)need.counters * sizeof(unsigned long long);
+        const bool fresh = !h->tc_counters || h->tc_counters_bytes < cbytes;
+        rc = ensure_buffer(reinterpret_cast<void**>(&h->tc_counters), &h->tc_counters_bytes, cbytes);
+        if (rc != GEMM_OK) return rc;
+        if (++h->tc_seq == 0) h->tc_seq = 1;
+        if ((fresh || h->tc_seq == 1) && cudaMemsetAsync(h->tc_counters, 0, h->tc_counters_bytes, s) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        t.rem_ws = h->workspace;
+        t.rem_cnt = h->tc_counters;
+        t.rem_seq = h->tc_seq;
+    }
     int n = 0;
     int rc2 = launch_tc_gemm(t, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_tc_chunk, h->opt_tc_pair, s, &n);
     h->launches += n;

@@ -105,7 +105,18 @@ struct TcArgs {
     int is_bf16;     // 1 = bf16, 0 = fp16
     int test_stall;  // test hook: make a bounded wait run out (exercises the timeout path)
     Epilogue epi;
+    // CTA-pair kernel, K split of the last wave's tiles (sizes from tc_workspace_need;
+    // null: no split)
+    float* rem_ws = nullptr;                  // partial tiles
+    unsigned long long* rem_cnt = nullptr;    // arrival counters, zeroed when allocated
+    unsigned rem_seq = 0;                     // a nonzero tag no earlier launch on rem_cnt used
 };
+struct TcWorkspace {
+    int64_t floats = 0;    // partial-tile floats
+    int64_t counters = 0;  // 64-bit arrival counters
+};
+// What launch_tc_gemm with these arguments would use to split its last wave (zero: none).
+TcWorkspace tc_workspace_need(const TcArgs& a, int num_sms, int pair_mode);
 // Returns GEMM_OK or a negative gemm_status_t.
 // kc_blocks: 64-wide k-blocks per accumulation chunk (0 = default 16).
 // pair_mode: 0 = choose, 1 = single-CTA 128 x 256 tiles, 2 = CTA-pair 256 x 256 tiles,

@@ -123,6 +123,13 @@ struct TcParams {
                   // (work item = tile * nsplit + slice); 1 = no split.  Slice z covers
                   // k-blocks [z * k_blocks / nsplit, (z + 1) * k_blocks / nsplit)
     int group_m;  // tile rows per raster group
+    // CTA-pair kernel, last-wave split: work items [0, rem_first) are whole tiles; the
+    // tiles from rem_first on are cut into rem_split K slices, item rem_first + j being
+    // slice j % rem_split of tile rem_first + j / rem_split.  rem_split = 1: no split.
+    int num_items, rem_first, rem_split;
+    float* rem_ws;                  // [tile - rem_first][slice][CTA][warp][4096] partials
+    unsigned long long* rem_cnt;    // [tile - rem_first][CTA][warp] arrivals, tagged rem_seq
+    uint32_t rem_seq;               // this launch's tag (nonzero)
     uint32_t idesc;
     int vec_store;
     int* status;
@@ -226,16 +233,91 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tmC, const flo
     }
 }
 
-__device__ __forceinline__ int slice_begin(const TcParams& p, int z)
-{
-    return (int)((int64_t)z * p.k_blocks / p.nsplit);
-}
-
 __device__ __forceinline__ void record_error(int* status, int code, volatile int* abort_flag)
 {
     atomicCAS(status, 0, code);
     *abort_flag = 1;
 }
+
+// A work item of the CTA-pair kernel: tile t, k-blocks [kb0, kb1), K slice sl (-1: whole).
+struct PairItem {
+    int t, sl, kb0, kb1;
+};
+
+__device__ __forceinline__ PairItem pair_item(const TcParams& p, int it)
+{
+    if (it < p.rem_first) return {it, -1, 0, p.k_blocks};
+    const int j = it - p.rem_first, sl = j % p.rem_split;
+    return {p.rem_first + j / p.rem_split, sl, (int)((int64_t)sl * p.k_blocks / p.rem_split),
+            (int)((int64_t)(sl + 1) * p.k_blocks / p.rem_split)};
+}
+
+constexpr int MAX_REM_SPLIT = 4;
+constexpr int REM_PART_FLOATS = 32 * EPI_COLS;  // one epilogue warp's 32 rows x 128 columns
+
+// Count one finished K slice of a tile part; returns the number of slices finished so far
+// in this launch (0 if the update kept failing).  The counter's upper half holds the launch
+// tag: a count left by another launch (one that stopped early) restarts at 1.
+__device__ __forceinline__ int slice_arrive(unsigned long long* counter, uint32_t seq)
+{
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(counter);
+    for (int i = 0; i < (1 << 20); ++i) {
+        const unsigned long long nxt =
+            ((uint32_t)(cur >> 32) == seq) ? cur + 1 : (((unsigned long long)seq << 32) | 1ull);
+        const unsigned long long prev = atomicCAS(counter, cur, nxt);
+        if (prev == cur) return (int)(uint32_t)nxt;
+        cur = prev;
+    }
+    return 0;
+}
+
+// Last-wave split, one epilogue warp's part (32 rows x 128 columns, thread = row) of K
+// slice `sl` of split tile j: publish it, count it, and if it is the part's last slice to
+// finish, replace `tot` by the sum of all slices in slice order (true: store C).  Nothing
+// waits for another warp or CTA.
+__device__ __forceinline__ bool rem_slice_combine(const TcParams& p, float (&tot)[EPI_COLS], int j, int sl, int cta,
+                                                  int w, int lane, int* status, volatile int* abort_flag)
+{
+    const int S = p.rem_split;
+    float* base = p.rem_ws + ((int64_t)(j * S) * 2 * EPI_WARPS + cta * EPI_WARPS + w) * REM_PART_FLOATS;
+    const int64_t zstride = (int64_t)2 * EPI_WARPS * REM_PART_FLOATS;  // between slices
+    float4* mine = reinterpret_cast<float4*>(base + sl * zstride) + lane;
+#pragma unroll
+    for (int q = 0; q < EPI_COLS / 4; ++q)
+        __stcg(mine + q * 32, make_float4(tot[4 * q], tot[4 * q + 1], tot[4 * q + 2], tot[4 * q + 3]));
+    __threadfence();
+    __syncwarp();
+    int n = 0;
+    if (lane == 0) {
+        n = slice_arrive(p.rem_cnt + ((int64_t)j * 2 + cta) * EPI_WARPS + w, p.rem_seq);
+        if (n == 0) record_error(status, kDevTimeoutEpilogue, abort_flag);
+    }
+    n = __shfl_sync(0xffffffffu, n, 0);
+    if (n != S) return false;
+    __threadfence();
+    // every slice, this warp's own included, is read back, so that no partial stays live
+    // in registers while the slices are added
+    const float4* src = reinterpret_cast<const float4*>(base) + lane;
+#pragma unroll
+    for (int q = 0; q < EPI_COLS / 4; ++q) {
+        float4 acc = __ldcg(src + q * 32);
+#pragma unroll
+        for (int z = 1; z < MAX_REM_SPLIT; ++z)
+            if (z < S) {
+                const float4 u = __ldcg(src + z * (zstride / 4) + q * 32);
+                acc.x = __fadd_rn(acc.x, u.x), acc.y = __fadd_rn(acc.y, u.y);
+                acc.z = __fadd_rn(acc.z, u.z), acc.w = __fadd_rn(acc.w, u.w);
+            }
+        tot[4 * q] = acc.x, tot[4 * q + 1] = acc.y, tot[4 * q + 2] = acc.z, tot[4 * q + 3] = acc.w;
+    }
+    return true;
+}
+
+__device__ __forceinline__ int slice_begin(const TcParams& p, int z)
+{
+    return (int)((int64_t)z * p.k_blocks / p.nsplit);
+}
+
 
 // Split-K output: this CTA (rank r of the tile's cluster of S slices) adds, for its share
 // of the tile's 16-byte chunks, the S partial tiles in slice order (read from each CTA's
@@ -738,9 +820,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = pair; t < p.num_tiles && ok; t += npairs) {
-                const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks, p.group_m);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+            for (int it = pair; it < p.num_items && ok; it += npairs) {
+                const PairItem w = pair_item(p, it);
+                const TileCoord tc = tile_coord(w.t, p.m_blocks, p.n_blocks, p.group_m);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait_cluster(smem_u32(&empty_bar[stage]), phase ^ 1, p.limit_ns, abort_flag)) {
                         record_error(p.status, kDevTimeoutProducer, abort_flag);
                         ok = false;
@@ -785,8 +868,11 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             bool ok = true;
             const uint32_t a_base = smem_u32(smem_a), b_base = smem_u32(smem_b);
             const uint32_t idesc = p.idesc;
-            for (int t = pair; t < p.num_tiles && ok; t += npairs) {
+            for (int it = pair; it < p.num_items && ok; it += npairs) {
+                const PairItem w = pair_item(p, it);
                 for (int ch = 0; ch < p.nchunks && ok; ++ch) {
+                    const int kb0 = w.kb0 + ch * p.kc;
+                    if (kb0 >= w.kb1) break;  // a K slice has fewer chunks
                     if (!mbar_wait_cluster(smem_u32(&tempty_bar[buf]), buf_phase ^ 1, p.limit_ns, abort_flag)) {
                         record_error(p.status, kDevTimeoutMma, abort_flag);
                         ok = false;
@@ -794,8 +880,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-                    const int kb0 = ch * p.kc;
-                    const int kb1 = min(kb0 + p.kc, p.k_blocks);
+                    const int kb1 = min(kb0 + p.kc, w.kb1);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait_cluster(smem_u32(&full_bar[stage]), phase, p.limit_ns, abort_flag)) {
                             record_error(p.status, kDevTimeoutMma, abort_flag);
@@ -849,11 +934,16 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             ok = __all_sync(0xffffffffu, ok);
             if (!ok && lane == 0) record_error(p.status, kDevTimeoutEpilogue, abort_flag);
             aborted = true;
-            t_first = p.num_tiles;
+            t_first = p.num_items;
         }
-        for (int t = t_first; t < p.num_tiles; t += npairs) {
+        for (int it = t_first; it < p.num_items; it += npairs) {
+            const PairItem w = pair_item(p, it);
+            const int t = w.t;
             bool ok = true;
+#pragma unroll
+            for (int i = 0; i < EPI_COLS; ++i) tot[i] = 0.f;  // (no value lives on from the last item)
             for (int ch = 0; ch < p.nchunks; ++ch) {
+                if (w.kb0 + ch * p.kc >= w.kb1) break;  // as the MMA issuer
                 ok = mbar_wait_cluster(smem_u32(&tfull_bar[buf]), buf_phase, p.limit_ns, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
@@ -888,6 +978,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 aborted = true;
                 break;
             }
+            // a K slice of a last-wave tile: only the part's last slice to finish stores C
+            if (w.sl >= 0 && !rem_slice_combine(p, tot, t - p.rem_first, w.sl, (int)rank, warp - 2, lane, p.status,
+                                                abort_flag))
+                continue;
             const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks, p.group_m);
             const int row = (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM + q * 32 + lane;
             if (p.c_tma) {
@@ -1032,6 +1126,95 @@ int choose_split(int64_t tiles, int64_t k_blocks, int num_sms)
 
 }  // namespace
 
+namespace {
+
+// Clusters of the CTA-pair kernel (PAIRS pairs each) resident at once (0: unknown).
+template <int PAIRS>
+int pair_clusters_fit()
+{
+    static std::atomic<int> cache{-1};
+    int v = cache.load();
+    if (v >= 0) return v;
+    v = 0;
+    auto kern = tc_gemm_pair_kernel<P_STAGES_DEFAULT, PAIRS>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem_bytes(P_STAGES_DEFAULT)) ==
+        cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * PAIRS, 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = p_smem_bytes(P_STAGES_DEFAULT);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2 * PAIRS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess) v = 0;
+    }
+    cudaGetLastError();
+    cache.store(v);
+    return v;
+}
+
+// How a product is laid on the tensor-core kernels.
+struct TcPlan {
+    bool pair = false, quad = false;
+    int64_t tiles = 0;    // output tiles of the chosen kernel
+    int clusters = 0;     // pair kernels: clusters launched
+    int rem_first = 0;    // pair kernel: first split tile (tiles = none)
+    int rem_split = 1;    // pair kernel: K slices of each last-wave tile
+};
+
+TcPlan plan_tc(const TcArgs& a, int num_sms, int pair_mode)
+{
+    TcPlan pl;
+    pl.quad = (pair_mode == 3) && num_sms >= 4;
+    pl.pair = pl.quad || (pair_mode == 2) || (pair_mode == 0 && a.M > BM && num_sms >= 2);
+    const int64_t n_blocks = (a.N + BN - 1) / BN;
+    if (!pl.pair) {
+        pl.tiles = ((a.M + BM - 1) / BM) * n_blocks;
+        return pl;
+    }
+    const int cl = pl.quad ? 4 : 2;
+    pl.tiles = ((a.M + cl * BM - 1) / (cl * BM)) * n_blocks;
+    int64_t clusters = pl.tiles < num_sms / cl ? pl.tiles : num_sms / cl;
+    // a persistent grid must be co-resident: clusters are placed within one GPC each, so
+    // fewer than num_sms / cl of them may fit
+    const int fit = pl.quad ? pair_clusters_fit<2>() : pair_clusters_fit<1>();
+    if (fit > 0 && fit < clusters) clusters = fit;
+    pl.clusters = (int)clusters;
+    pl.rem_first = (int)pl.tiles;
+    // the tiles of a last wave that leaves pairs idle are cut along K (CTA pairs only;
+    // the stall hook runs unsplit).  Adding a tile's slices costs about 7 us (each part
+    // published to L2, counted, the others read back), so every slice keeps at least 32
+    // k-blocks (about 11 us of MMAs on a pair): shorter slices measured slower than none.
+    const int64_t r = pl.tiles % clusters;
+    const int64_t k_blocks = (a.K + BK - 1) / BK;
+    if (pl.quad || a.test_stall || r == 0) return pl;
+    int64_t sp = clusters / r;
+    if (sp > MAX_REM_SPLIT) sp = MAX_REM_SPLIT;
+    while (sp > 1 && k_blocks / sp < 32) --sp;
+    if (sp < 2) return pl;
+    pl.rem_first = (int)(pl.tiles - r);
+    pl.rem_split = (int)sp;
+    return pl;
+}
+
+}  // namespace
+
+TcWorkspace tc_workspace_need(const TcArgs& a, int num_sms, int pair_mode)
+{
+    TcWorkspace w;
+    if (a.M <= 0 || a.N <= 0 || a.K <= 0) return w;
+    const TcPlan pl = plan_tc(a, num_sms, pair_mode);
+    if (pl.rem_split < 2) return w;
+    const int64_t split_tiles = pl.tiles - pl.rem_first;
+    w.floats = split_tiles * pl.rem_split * 2 * EPI_WARPS * REM_PART_FLOATS;
+    w.counters = split_tiles * 2 * EPI_WARPS;
+    return w;
+}
+
 int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_limit_ns, int kc_blocks,
                    int pair_mode, cudaStream_t stream, int* launches)
 {
@@ -1078,16 +1261,32 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.test_stall = a.test_stall;
     // CTA pairs: 256 x 256 tiles on clusters of two (or 512 x 256 tiles on clusters of
     // two pairs sharing B); single CTAs: 128 x 256 tiles
-    const bool use_quad = (pair_mode == 3) && num_sms >= 4;
-    const bool use_pair = use_quad || (pair_mode == 2) || (pair_mode == 0 && a.M > BM && num_sms >= 2);
-    if (use_pair) {
+    const TcPlan pl = plan_tc(a, num_sms, pair_mode);
+    const bool use_quad = pl.quad;
+    p.num_items = p.num_tiles;
+    p.rem_first = p.num_tiles;
+    p.rem_split = 1;
+    p.rem_ws = nullptr;
+    p.rem_cnt = nullptr;
+    p.rem_seq = 0;
+    if (pl.pair) {
         const int pairs_per_cluster = use_quad ? 2 : 1;
         const int cl = 2 * pairs_per_cluster;  // CTAs per cluster
         p.m_blocks = (int)((a.M + cl * BM - 1) / (cl * BM));
         const int64_t ctiles = (int64_t)p.m_blocks * p.n_blocks;
         p.num_tiles = (int)ctiles;
+        p.num_items = p.num_tiles;
+        p.rem_first = p.num_tiles;
+        if (pl.rem_split > 1 && a.rem_ws && a.rem_cnt && a.rem_seq) {
+            p.rem_first = pl.rem_first;
+            p.rem_split = pl.rem_split;
+            p.num_items = pl.rem_first + (p.num_tiles - pl.rem_first) * pl.rem_split;
+            p.rem_ws = a.rem_ws;
+            p.rem_cnt = a.rem_cnt;
+            p.rem_seq = a.rem_seq;
+        }
         p.idesc = make_idesc(bf16, 2 * BM);
-        const int clusters = (int)(ctiles < num_sms / cl ? ctiles : num_sms / cl);
+        const int clusters = pl.clusters;
         // 6 stages of 32 KiB; 7 measured no faster.  Raster groups of 2048 rows of C
         // (8 pair tiles) measured best among 512 .. 4096 rows, within run-to-run noise.
         constexpr int stages = P_STAGES_DEFAULT;
@@ -1111,11 +1310,6 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        // a persistent grid must be co-resident: clusters are placed within one GPC each,
-        // so fewer than num_sms / cl of them may fit
-        int fit = 0;
-        if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < clusters)
-            cfg.gridDim = dim3(cl * fit, 1, 1);
         if (cudaLaunchKernelEx(&cfg, kern, tmA, use_quad ? tmBq : tmB, tmC, p) != cudaSuccess) return GEMM_ERR_CUDA;
         *launches += 1;
         return GEMM_OK;

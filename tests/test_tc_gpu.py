@@ -105,18 +105,49 @@ def test_normal_bf16_within_tolerance(lib, pair, M, N, K):
     assert err <= 2e-5 * math.sqrt(K), err
 
 
-def test_results_are_deterministic(lib):
+@pytest.mark.parametrize("M,N,K", [(1024, 2048, 2048), (4096, 4096, 2048)])
+def test_results_are_deterministic(lib, M, N, K):
+    """Every kernel family repeats its result bit for bit.  The families agree within the
+    tolerance: the CTA-pair kernel may cut a last wave's tiles along K, which regroups the
+    chunk sums of those tiles."""
     import programming_tiled_gemm_gb300 as g
-    A, B = si.gemm_operands(1024, 2048, 2048, seed=5, dist="normal", dtype="bf16")
+    A, B = si.gemm_operands(M, N, K, seed=5, dist="normal", dtype="bf16")
     Ad, Bd = A.cuda(), B.cuda()
-    c1 = lib.matmul(Ad, Bd).clone()
-    c2 = lib.matmul(Ad, Bd)
-    assert torch.equal(c1, c2)
-    # the single-CTA, pair and two-pair kernels sum the same products in the same chunk order
-    for pair in (1, 3):
+    ref = None
+    for pair in (0, 1, 2, 3):
         lib.set_option(g.GEMM_OPT_TC_PAIR, pair)
-        c3 = lib.matmul(Ad, Bd)
-        assert torch.equal(c1, c3)
+        c1 = lib.matmul(Ad, Bd).clone()
+        for _ in range(2):
+            assert torch.equal(c1, lib.matmul(Ad, Bd)), pair
+        if ref is None:
+            ref = c1
+        assert (c1 - ref).abs().max().item() <= 2 * 2e-5 * math.sqrt(K)
+
+
+LAST_WAVE_SHAPES = [  # CTA-pair tiles (256 x 256) whose last wave is cut along K (76 pairs)
+    (4096, 4096, 4096),   # 256 tiles: 228 whole, the last 28 in 2 slices
+    (3072, 2048, 6144),   # 96 tiles: the last 20 in 3 slices of 32 k-blocks
+    (1024, 1024, 8192),   # 16 tiles, all in 4 slices
+    (1000, 1000, 8400),   # ragged M, N and K: slices of 32 and 33 k-blocks, a partial k-block
+    (1024, 2048, 4096),   # 32 tiles, all in 2 slices
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", LAST_WAVE_SHAPES)
+def test_last_wave_split_integer_inputs_exact(lib, dtype, M, N, K):
+    """The CTA-pair kernel's last-wave tiles run as K slices; the warp finishing a tile
+    part's last slice adds the slices' partials in slice order and stores C."""
+    A, B = si.integer_copy(M, N, K, seed=M + 7 * N + K, dtype=dtype)
+    got = run_guarded(lib, A, B)
+    assert np.array_equal(got, oracle.gemm(A.float().numpy(), B.float().numpy()))
+
+
+def test_last_wave_split_within_tolerance(lib):
+    A, B = si.gemm_operands(4096, 4096, 4096, seed=41, dist="normal", dtype="bf16")
+    got = run_guarded(lib, A, B)
+    err = np.abs(got - oracle.gemm(A.float().numpy(), B.float().numpy())).max()
+    assert err <= 2e-5 * math.sqrt(4096), err
 
 
 SPLIT_SHAPES = [  # M <= 128 with 128 x 256 tiles filling under half the SMs: K is split
