@@ -30,7 +30,8 @@
  *
  * Threads: a handle is not thread-safe.  Use one handle per host thread, or serialise
  * calls.  Calls on one handle from different streams must not overlap in time when
- * they use the split-K workspace (fp32 shapes with small M or few output tiles).
+ * they use the split-K workspace (fp32 shapes with small M or few output tiles; bf16 /
+ * fp16 shapes whose last wave of 256 x 256 tiles is cut along K).
  *
  * Errors: every entry point returns a gemm_status_t (0 = success, negative = error)
  * and writes nothing when it fails its argument checks.
@@ -80,7 +81,9 @@ int gemm_destroy(gemm_handle_t h);
  *   lda, ldb multiples of 8 elements (TMA tensor-map rules), else GEMM_ERR_ALIGNMENT.
  *   C (float*) needs no alignment beyond 4 bytes.
  *   stream: cudaStream_t (NULL = legacy default stream).  Asynchronous.
- * Kernel choice is by shape and dtype among this library's own kernels only. */
+ * Kernel choice is by shape and dtype among this library's own kernels only.  Results
+ * are deterministic: the same call on the same device repeats its result bit for bit
+ * (every split of K adds its slices in a fixed order). */
 int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
              const void* A, int64_t lda, const void* B, int64_t ldb,
              float* C, int64_t ldc, gemm_dtype_t dtype, void* stream);
