@@ -356,21 +356,30 @@ HostStage host_stage_layout(const gemm_host_problem& q, size_t base)
     return st;
 }
 
-// Row chunks of one host problem: 16-bit inputs are transfer-bound (the tensor cores
-// outrun a ~200 GB/s host link), so they take up to 8 chunks of >= 1024 rows; fp32 is
-// compute-bound, so 2 chunks of >= 2048 rows keep its launches full.
-void host_chunks(const gemm_host_problem& q, int64_t* chunk, int* nchunks)
+// Row chunks of one host problem, in order.
+//   16-bit inputs are transfer-bound (the tensor cores outrun a ~200 GB/s host link):
+//   2 to 4 chunks of >= 1024 rows, 4096 and more where M allows, so that each launch
+//   keeps several waves of 256 x 256 tiles (measured at 8192^3: four 2048-row chunks
+//   computed in 0.72 ms, one launch in 0.63 ms).
+//   fp32 is compute-bound: one half of the rows, then three eighths, then one eighth.
+//   The batch's last piece of work then has a small result to bring back.
+std::vector<int64_t> host_chunk_rows(const gemm_host_problem& q)
 {
-    *chunk = q.M;
-    *nchunks = (q.M > 0 && q.N > 0) ? 1 : 0;
-    const int64_t min_rows = (q.dtype == GEMM_F32) ? 2048 : 1024;
-    const int max_chunks = (q.dtype == GEMM_F32) ? 2 : gemm_ctx::kMaxChunks;
-    if (q.K > 0 && q.N > 0 && q.M >= 2 * min_rows) {
-        int n = (int)(q.M / min_rows);
-        if (n > max_chunks) n = max_chunks;
-        *chunk = ((q.M + n - 1) / n + 255) / 256 * 256;
-        *nchunks = (int)((q.M + *chunk - 1) / *chunk);
+    std::vector<int64_t> rows;
+    if (q.M <= 0 || q.N <= 0) return rows;
+    auto up256 = [](int64_t v) { return (v + 255) / 256 * 256; };
+    if (q.K > 0 && q.dtype == GEMM_F32 && q.M >= 4096) {
+        const int64_t a = up256(q.M / 2), b = up256(q.M * 3 / 8);
+        rows = {a, b, q.M - a - b};
+    } else if (q.K > 0 && q.dtype != GEMM_F32 && q.M >= 2048) {
+        int64_t n = q.M / 4096;
+        n = n < 2 ? 2 : (n > 4 ? 4 : n);
+        const int64_t c = up256((q.M + n - 1) / n);
+        for (int64_t m0 = 0; m0 < q.M; m0 += c) rows.push_back(q.M - m0 < c ? q.M - m0 : c);
+    } else {
+        rows = {q.M};
     }
+    return rows;
 }
 
 // A problem whose estimated compute time exceeds its estimated transfer time (rates of
@@ -450,24 +459,30 @@ int run_host_problems(gemm_handle_t h, int count, const gemm_host_problem* q, vo
         st[i] = host_stage_layout(q[i], off);
         off += st[i].bytes;
     }
-    // Chunk order on the compute stream: half of the compute-bound problems' chunks, then
-    // the transfer-bound problems' chunks, then the rest.  The first compute starts after
-    // a short upload, the transfer-bound chunks' copies hide under compute on both sides,
-    // and the last chunk's result is short to bring back.  Chunks of one problem keep
-    // their order (its B goes in before its first chunk).
+    // Chunk order on the compute stream: the compute-bound problems' chunks up to half of
+    // their work, then the transfer-bound problems' chunks, then the rest.  The first
+    // compute starts after a short upload, the transfer-bound chunks' copies hide under
+    // compute on both sides, and the last chunk's result is short to bring back.  Chunks
+    // of one problem keep their order (its B goes in before its first chunk).
     std::vector<HostChunk> cb, tb;
+    double cb_work = 0.0;
     for (int i = 0; i < count; ++i) {
-        int64_t chunk;
-        int n;
-        host_chunks(q[i], &chunk, &n);
-        for (int c = 0; c < n; ++c) {
-            const int64_t m0 = c * chunk, rows = (q[i].M - m0) < chunk ? (q[i].M - m0) : chunk;
-            (compute_bound(q[i]) ? cb : tb).push_back({i, m0, rows});
+        const bool bound = compute_bound(q[i]);
+        int64_t m0 = 0;
+        for (const int64_t rows : host_chunk_rows(q[i])) {
+            (bound ? cb : tb).push_back({i, m0, rows});
+            if (bound) cb_work += (double)rows * (double)q[i].N * (double)q[i].K;
+            m0 += rows;
         }
     }
-    std::vector<HostChunk> order(cb.begin(), cb.begin() + (cb.size() + 1) / 2);
+    // compute-bound chunks up to half of their work go first, then the transfer-bound
+    // ones, then the rest
+    size_t first = 0;
+    for (double done = 0.0; first < cb.size() && done < 0.5 * cb_work; ++first)
+        done += (double)cb[first].rows * (double)q[cb[first].prob].N * (double)q[cb[first].prob].K;
+    std::vector<HostChunk> order(cb.begin(), cb.begin() + first);
     order.insert(order.end(), tb.begin(), tb.end());
-    order.insert(order.end(), cb.begin() + (cb.size() + 1) / 2, cb.end());
+    order.insert(order.end(), cb.begin() + first, cb.end());
     std::vector<char> started(count, 0);
     for (size_t k = 0; k < order.size(); ++k) {
         const HostChunk& c = order[k];
