@@ -277,21 +277,24 @@ int gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha, c
     }
     TcArgs t{M, N, K, A, lda, B, ldb, C, ldc, ab_dtype == GEMM_BF16 ? 1 : 0, h->opt_test_stall, epi};
     const TcWorkspace need = tc_workspace_need(t, h->num_sms, h->opt_tc_pair);
-    if (need.floats > 0) {
-        rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes,
-                           (size_t)need.floats * sizeof(float));
-        if (rc != GEMM_OK) return rc;
-        // arrival counters: zeroed when (re)allocated and when the launch tag wraps; a
-        // launch trusts only counts that carry its own tag
-        const size_t cbytes = (size_t)need.counters * sizeof(unsigned long long);
+    if (need.counters > 0) {
+        if (need.floats > 0) {
+            rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes,
+                               (size_t)need.floats * sizeof(float));
+            if (rc != GEMM_OK) return rc;
+            t.rem_ws = h->workspace;
+        }
+        // arrival counters and publication flags: zeroed when (re)allocated and when the
+        // launch tag wraps; a launch trusts only values that carry its own tag
+        const size_t cbytes = (size_t)need.counters * (sizeof(unsigned long long) + sizeof(uint32_t));
         const bool fresh = !h->tc_counters || h->tc_counters_bytes < cbytes;
         rc = ensure_buffer(reinterpret_cast<void**>(&h->tc_counters), &h->tc_counters_bytes, cbytes);
         if (rc != GEMM_OK) return rc;
         if (++h->tc_seq == 0) h->tc_seq = 1;
         if ((fresh || h->tc_seq == 1) && cudaMemsetAsync(h->tc_counters, 0, h->tc_counters_bytes, s) != cudaSuccess)
             return GEMM_ERR_CUDA;
-        t.rem_ws = h->workspace;
         t.rem_cnt = h->tc_counters;
+        t.rem_flag = reinterpret_cast<uint32_t*>(h->tc_counters + need.counters);
         t.rem_seq = h->tc_seq;
     }
     int n = 0;

@@ -107,13 +107,14 @@ struct TcArgs {
     Epilogue epi;
     // CTA-pair kernel, K split of the last wave's tiles (sizes from tc_workspace_need;
     // null: no split)
-    float* rem_ws = nullptr;                  // partial tiles
+    float* rem_ws = nullptr;                  // partial tiles (when TcWorkspace::floats > 0)
     unsigned long long* rem_cnt = nullptr;    // arrival counters, zeroed when allocated
-    unsigned rem_seq = 0;                     // a nonzero tag no earlier launch on rem_cnt used
+    uint32_t* rem_flag = nullptr;             // publication flags, as many, zeroed when allocated
+    unsigned rem_seq = 0;                     // a nonzero tag no earlier launch on them used
 };
 struct TcWorkspace {
     int64_t floats = 0;    // partial-tile floats
-    int64_t counters = 0;  // 64-bit arrival counters
+    int64_t counters = 0;  // 64-bit arrival counters, and as many 32-bit flags
 };
 // What launch_tc_gemm with these arguments would use to split its last wave (zero: none).
 TcWorkspace tc_workspace_need(const TcArgs& a, int num_sms, int pair_mode);

@@ -129,7 +129,9 @@ struct TcParams {
     int num_items, rem_first, rem_split;
     float* rem_ws;                  // [tile - rem_first][slice][CTA][warp][4096] partials
     unsigned long long* rem_cnt;    // [tile - rem_first][CTA][warp] arrivals, tagged rem_seq
+    uint32_t* rem_flag;             // [same] rem_seq once the first slice's part is in C
     uint32_t rem_seq;               // this launch's tag (nonzero)
+    int rem_direct;                 // 2 slices, plain fp32 C by TMA: C = first, then += second
     uint32_t idesc;
     int vec_store;
     int* status;
@@ -211,6 +213,7 @@ __device__ __forceinline__ void epi_store4(const TcParams& p, int64_t off, int n
 // layout of tmC's box (16-byte chunk c of row r at chunk c ^ (r & 7): the row-per-thread
 // writes meet no bank conflicts), then one TMA store of full 128-byte row segments.  The
 // TMA clips rows past M and columns past N.
+template <bool ADD = false>
 __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tmC, const float (&tot)[EPI_COLS], uint8_t* stg,
                                                int row0, int col0, int M, int N, int lane)
 {
@@ -227,7 +230,10 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tmC, const flo
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d(tmC, smem_u32(stg), col0 + 32 * j, row0);
+            if (ADD)
+                tma_reduce_add_2d(tmC, smem_u32(stg), col0 + 32 * j, row0);
+            else
+                tma_store_2d(tmC, smem_u32(stg), col0 + 32 * j, row0);
             bulk_commit_group();
         }
     }
@@ -978,11 +984,55 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 aborted = true;
                 break;
             }
+            const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks, p.group_m);
+            if (w.sl >= 0 && p.rem_direct) {
+                // a last-wave tile in two K slices, plain fp32 C: the part's first slice to
+                // finish stores it, the second adds itself in L2 (a + b = b + a: the same
+                // bits whichever comes first)
+                const int64_t part = ((int64_t)(t - p.rem_first) * 2 + rank) * EPI_WARPS + (warp - 2);
+                int n = 0;
+                if (lane == 0) {
+                    n = slice_arrive(p.rem_cnt + part, p.rem_seq);
+                    if (n == 0) record_error(p.status, kDevTimeoutEpilogue, abort_flag);
+                }
+                n = __shfl_sync(0xffffffffu, n, 0);
+                uint8_t* stg = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
+                const int row0 = (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM + q * 32;
+                const int col0 = tc.n_blk * BN + half * EPI_COLS;
+                if (n == 1) {
+                    store_rows_tma<false>(&tmC, tot, stg, row0, col0, p.M, p.N, lane);
+                    if (lane == 0) {
+                        bulk_wait_group0();  // the part is in C
+                        fence_proxy_async_global();
+                        __threadfence();
+                        st_release_gpu(p.rem_flag + part, p.rem_seq);
+                    }
+                    __syncwarp();
+                } else if (n == 2) {
+                    // the first slice's warp has counted itself, so it is running and
+                    // publishes without waiting on anything; the wait is bounded all the same
+                    bool ok2 = true;
+                    if (lane == 0) {
+                        const uint64_t t0 = global_timer();
+                        while (ld_acquire_gpu(p.rem_flag + part) != p.rem_seq) {
+                            if (*abort_flag || global_timer() - t0 > p.limit_ns) {
+                                record_error(p.status, kDevTimeoutEpilogue, abort_flag);
+                                ok2 = false;
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                        fence_proxy_async_global();
+                    }
+                    ok2 = __shfl_sync(0xffffffffu, ok2 ? 1 : 0, 0) != 0;
+                    if (ok2) store_rows_tma<true>(&tmC, tot, stg, row0, col0, p.M, p.N, lane);
+                }
+                continue;
+            }
             // a K slice of a last-wave tile: only the part's last slice to finish stores C
             if (w.sl >= 0 && !rem_slice_combine(p, tot, t - p.rem_first, w.sl, (int)rank, warp - 2, lane, p.status,
                                                 abort_flag))
                 continue;
-            const TileCoord tc = tile_coord(t, p.m_blocks, p.n_blocks, p.group_m);
             const int row = (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM + q * 32 + lane;
             if (p.c_tma) {
                 store_rows_tma(&tmC, tot, epi_stage + (warp - 2) * EPI_STAGE_BYTES, (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM + q * 32,
@@ -1164,11 +1214,14 @@ struct TcPlan {
     int clusters = 0;     // pair kernels: clusters launched
     int rem_first = 0;    // pair kernel: first split tile (tiles = none)
     int rem_split = 1;    // pair kernel: K slices of each last-wave tile
+    bool c_tma = false;   // plain fp32 C with 16-byte aligned rows: TMA stores
+    bool rem_direct = false;  // two slices added straight into C (no partial workspace)
 };
 
 TcPlan plan_tc(const TcArgs& a, int num_sms, int pair_mode)
 {
     TcPlan pl;
+    pl.c_tma = a.epi.plain() && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0;
     pl.quad = (pair_mode == 3) && num_sms >= 4;
     pl.pair = pl.quad || (pair_mode == 2) || (pair_mode == 0 && a.M > BM && num_sms >= 2);
     const int64_t n_blocks = (a.N + BN - 1) / BN;
@@ -1198,6 +1251,7 @@ TcPlan plan_tc(const TcArgs& a, int num_sms, int pair_mode)
     if (sp < 2) return pl;
     pl.rem_first = (int)(pl.tiles - r);
     pl.rem_split = (int)sp;
+    pl.rem_direct = (sp == 2) && pl.c_tma;
     return pl;
 }
 
@@ -1210,7 +1264,7 @@ TcWorkspace tc_workspace_need(const TcArgs& a, int num_sms, int pair_mode)
     const TcPlan pl = plan_tc(a, num_sms, pair_mode);
     if (pl.rem_split < 2) return w;
     const int64_t split_tiles = pl.tiles - pl.rem_first;
-    w.floats = split_tiles * pl.rem_split * 2 * EPI_WARPS * REM_PART_FLOATS;
+    w.floats = pl.rem_direct ? 0 : split_tiles * pl.rem_split * 2 * EPI_WARPS * REM_PART_FLOATS;
     w.counters = split_tiles * 2 * EPI_WARPS;
     return w;
 }
@@ -1268,7 +1322,9 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.rem_split = 1;
     p.rem_ws = nullptr;
     p.rem_cnt = nullptr;
+    p.rem_flag = nullptr;
     p.rem_seq = 0;
+    p.rem_direct = 0;
     if (pl.pair) {
         const int pairs_per_cluster = use_quad ? 2 : 1;
         const int cl = 2 * pairs_per_cluster;  // CTAs per cluster
@@ -1277,13 +1333,16 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
         p.num_tiles = (int)ctiles;
         p.num_items = p.num_tiles;
         p.rem_first = p.num_tiles;
-        if (pl.rem_split > 1 && a.rem_ws && a.rem_cnt && a.rem_seq) {
+        if (pl.rem_split > 1 && (pl.rem_direct || a.rem_ws) && a.rem_cnt && a.rem_flag && a.rem_seq &&
+            pl.c_tma == (p.c_tma != 0)) {
             p.rem_first = pl.rem_first;
             p.rem_split = pl.rem_split;
             p.num_items = pl.rem_first + (p.num_tiles - pl.rem_first) * pl.rem_split;
             p.rem_ws = a.rem_ws;
             p.rem_cnt = a.rem_cnt;
+            p.rem_flag = a.rem_flag;
             p.rem_seq = a.rem_seq;
+            p.rem_direct = pl.rem_direct ? 1 : 0;
         }
         p.idesc = make_idesc(bf16, 2 * BM);
         const int clusters = pl.clusters;

@@ -105,7 +105,7 @@ def test_normal_bf16_within_tolerance(lib, pair, M, N, K):
     assert err <= 2e-5 * math.sqrt(K), err
 
 
-@pytest.mark.parametrize("M,N,K", [(1024, 2048, 2048), (4096, 4096, 2048)])
+@pytest.mark.parametrize("M,N,K", [(1024, 2048, 2048), (4096, 4096, 4096)])
 def test_results_are_deterministic(lib, M, N, K):
     """Every kernel family repeats its result bit for bit.  The families agree within the
     tolerance: the CTA-pair kernel may cut a last wave's tiles along K, which regroups the
@@ -141,6 +141,25 @@ def test_last_wave_split_integer_inputs_exact(lib, dtype, M, N, K):
     A, B = si.integer_copy(M, N, K, seed=M + 7 * N + K, dtype=dtype)
     got = run_guarded(lib, A, B)
     assert np.array_equal(got, oracle.gemm(A.float().numpy(), B.float().numpy()))
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (1024, 2048, 4096), (1500, 1504, 4200)])
+def test_last_wave_two_slices_into_aligned_C_exact(lib, M, N, K):
+    """Two K slices and a plain fp32 C with 16-byte aligned rows: the part's first slice
+    to finish stores C (TMA), the second adds itself to C (TMA reduce-add).  The rows
+    around C and the padding past column N stay untouched."""
+    dev = torch.device("cuda")
+    A, B = si.integer_copy(M, N, K, seed=M + N + 3 * K, dtype="bf16")
+    ldc = (N + 4 + 3) // 4 * 4
+    big = torch.full((M + 2, ldc), SENTINEL, device=dev)
+    C = big[1:M + 1, :N]
+    lib.matmul(A.to(dev), B.to(dev), out=C)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    host = big.cpu()
+    assert torch.all(host[0] == SENTINEL) and torch.all(host[M + 1] == SENTINEL)
+    assert torch.all(host[1:M + 1, N:] == SENTINEL)
+    assert np.array_equal(host[1:M + 1, :N].double().numpy(), oracle.gemm(A.float().numpy(), B.float().numpy()))
 
 
 def test_last_wave_split_within_tolerance(lib):
