@@ -1163,9 +1163,9 @@ int split_clusters_fit(int S)
     return v;
 }
 
-// K slices for an M <= 128 product whose 128 x 256 tiles fill under half the SMs: the
-// largest power of two that keeps every slice at least 4 k-blocks deep, the grid within
-// the SMs and every tile's cluster resident at once.  1 = no split.
+// K slices for a product whose 128 x 256 tiles fill under half the SMs: the largest
+// power of two that keeps every slice at least 4 k-blocks deep, the grid within the SMs
+// and every tile's cluster resident at once.  1 = no split.
 int choose_split(int64_t tiles, int64_t k_blocks, int num_sms)
 {
     if (2 * tiles > num_sms) return 1;
@@ -1216,6 +1216,7 @@ struct TcPlan {
     int rem_split = 1;    // pair kernel: K slices of each last-wave tile
     bool c_tma = false;   // plain fp32 C with 16-byte aligned rows: TMA stores
     bool rem_direct = false;  // two slices added straight into C (no partial workspace)
+    int single_split = 1;     // single-CTA kernel: K slices per tile on a cluster (1 = none)
 };
 
 TcPlan plan_tc(const TcArgs& a, int num_sms, int pair_mode)
@@ -1225,33 +1226,42 @@ TcPlan plan_tc(const TcArgs& a, int num_sms, int pair_mode)
     pl.quad = (pair_mode == 3) && num_sms >= 4;
     pl.pair = pl.quad || (pair_mode == 2) || (pair_mode == 0 && a.M > BM && num_sms >= 2);
     const int64_t n_blocks = (a.N + BN - 1) / BN;
+    const int64_t k_blocks = (a.K + BK - 1) / BK;
+    const int64_t single_tiles = ((a.M + BM - 1) / BM) * n_blocks;
     if (!pl.pair) {
-        pl.tiles = ((a.M + BM - 1) / BM) * n_blocks;
+        pl.tiles = single_tiles;
+        // M <= 128 with few tiles (chosen tiles only; the stall hook runs unsplit)
+        if (pair_mode == 0 && !a.test_stall && a.M <= BM) pl.single_split = choose_split(single_tiles, k_blocks, num_sms);
         return pl;
     }
     const int cl = pl.quad ? 4 : 2;
     pl.tiles = ((a.M + cl * BM - 1) / (cl * BM)) * n_blocks;
-    int64_t clusters = pl.tiles < num_sms / cl ? pl.tiles : num_sms / cl;
     // a persistent grid must be co-resident: clusters are placed within one GPC each, so
     // fewer than num_sms / cl of them may fit
+    int64_t clusters = num_sms / cl;
     const int fit = pl.quad ? pair_clusters_fit<2>() : pair_clusters_fit<1>();
     if (fit > 0 && fit < clusters) clusters = fit;
-    pl.clusters = (int)clusters;
     pl.rem_first = (int)pl.tiles;
     // the tiles of a last wave that leaves pairs idle are cut along K (CTA pairs only;
     // the stall hook runs unsplit).  Adding a tile's slices costs about 7 us (each part
     // published to L2, counted, the others read back), so every slice keeps at least 32
     // k-blocks (about 11 us of MMAs on a pair): shorter slices measured slower than none.
-    const int64_t r = pl.tiles % clusters;
-    const int64_t k_blocks = (a.K + BK - 1) / BK;
-    if (pl.quad || a.test_stall || r == 0) return pl;
-    int64_t sp = clusters / r;
-    if (sp > MAX_REM_SPLIT) sp = MAX_REM_SPLIT;
-    while (sp > 1 && k_blocks / sp < 32) --sp;
-    if (sp < 2) return pl;
-    pl.rem_first = (int)(pl.tiles - r);
-    pl.rem_split = (int)sp;
-    pl.rem_direct = (sp == 2) && pl.c_tma;
+    const int64_t r = pl.tiles % clusters;  // tiles of the last wave (all of them if fewer than pairs)
+    if (!pl.quad && !a.test_stall && r != 0) {
+        int64_t sp = clusters / r;
+        if (sp > MAX_REM_SPLIT) sp = MAX_REM_SPLIT;
+        while (sp > 1 && k_blocks / sp < 32) --sp;
+        if (sp >= 2) {
+            pl.rem_first = (int)(pl.tiles - r);
+            pl.rem_split = (int)sp;
+            pl.rem_direct = (sp == 2) && pl.c_tma;
+        }
+    }
+    // (Small products with M > 128 stay on pairs even when the single-CTA kernel's K split
+    // would keep more SMs busy: its exchange through distributed shared memory costs about
+    // 10 us, more than it saves below ~10 GFLOP, e.g. 0.017 -> 0.019 ms at 1024^3.)
+    const int64_t items = pl.rem_first + (pl.tiles - pl.rem_first) * pl.rem_split;
+    pl.clusters = (int)(items < clusters ? items : clusters);
     return pl;
 }
 
@@ -1373,10 +1383,9 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
         *launches += 1;
         return GEMM_OK;
     }
-    // M <= 128 with few tiles (chosen tiles only; the stall hook runs unsplit): K slices
-    // of a tile on a cluster of CTAs, one slice each, added through distributed shared
-    // memory in slice order
-    const int S = (pair_mode == 0 && !a.test_stall && a.M <= BM) ? choose_split(tiles, p.k_blocks, num_sms) : 1;
+    // few tiles (see plan_tc): K slices of a tile on a cluster of CTAs, one slice each,
+    // added through distributed shared memory in slice order
+    const int S = pl.single_split;
     if (S > 1) {
         p.nsplit = S;
         const int depth = (p.k_blocks + S - 1) / S;  // the deepest slice
