@@ -324,7 +324,6 @@ __device__ __forceinline__ int slice_begin(const TcParams& p, int z)
     return (int)((int64_t)z * p.k_blocks / p.nsplit);
 }
 
-
 // Split-K output: this CTA (rank r of the tile's cluster of S slices) adds, for its share
 // of the tile's 16-byte chunks, the S partial tiles in slice order (read from each CTA's
 // shared memory) and stores C.  e = 0 .. EPI_THREADS - 1.
@@ -1132,6 +1131,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 namespace {
 
 // Clusters of `S` single-CTA kernels that can be resident at once (0: none), per size.
+// Cached per process: every device a process drives is taken to be the same part.
 int split_clusters_fit(int S)
 {
     static std::atomic<int> cache[MAX_SPLIT + 1];
@@ -1179,6 +1179,7 @@ int choose_split(int64_t tiles, int64_t k_blocks, int num_sms)
 namespace {
 
 // Clusters of the CTA-pair kernel (PAIRS pairs each) resident at once (0: unknown).
+// Cached per process: every device a process drives is taken to be the same part.
 template <int PAIRS>
 int pair_clusters_fit()
 {
