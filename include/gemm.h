@@ -200,7 +200,7 @@ int gemm_get_device_status(gemm_handle_t h, void* stream);
 /* Tuning and test options (see GEMM_OPT_*).  Values outside the documented range are
  * rejected with GEMM_ERR_INVALID_ARG.  Defaults are restored by passing 0. */
 typedef enum {
-    GEMM_OPT_F32_KERNEL = 1, /* 0 auto, 1 tiled 128x128 FFMA, 2 tiled 64x128 FFMA, 3 skinny streaming from
+    GEMM_OPT_F32_KERNEL = 1, /* 0 auto, 1 tiled 128x256 FFMA, 2 tiled 64x128 FFMA, 3 skinny streaming from
                                 registers (M<=32), 4 skinny streaming through a TMA ring (M<=32; B 16-byte
                                 aligned with ldb % 4 == 0, else GEMM_ERR_ALIGNMENT) */
     GEMM_OPT_SPLIT_K = 2,    /* 0 auto, else the split-K factor for fp32 kernels (1..1024) */

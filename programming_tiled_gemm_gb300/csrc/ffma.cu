@@ -8,11 +8,12 @@
 //  * section "Why does tiling work?": neighbouring threads read neighbouring addresses
 //    (128-byte transactions) -- here every global access is a float4;
 //  * section "Improving the solution and balancing memory work": every thread owns a 2-D
-//    block of accumulators (TM x TN, the page's WPTM x WPTN = 8 x 8) and runs an outer
-//    product per k from registers: one A value times a row of B values, no shuffles;
+//    block of accumulators (TM x TN; the page's WPTM x WPTN = 8 x 8, here 8 x 16) and runs
+//    an outer product per k from registers: one A value times a row of B values, no
+//    shuffles;
 //  * section "How to do even better": rectangular tiles, A stored transposed (k-major)
 //    in shared memory, rows padded against bank conflicts.
-// What differs from the page: the tile is 128 x 128 x 8 (or 64 x 128 x 16) for 256
+// What differs from the page: the tile is 128 x 256 x 16 (or 64 x 128 x 16) for 256
 // threads, global loads for tile t+1 are in flight while tile t is multiplied (two
 // shared buffers, one barrier per tile), M/N/K tails are predicated (zero fill), and an
 // optional split of K over grid.z with a fixed-order reduction fills the GPU when there
@@ -212,19 +213,21 @@ ffma_tiled_kernel(F32Args p, int64_t k_per_split, int m_tiles, int n_tiles, floa
     }
 }
 
-// 128 x 128 x 16 block tile, 256 threads as 2 x 4 warps of 64 x 32; inside a warp the
-// lanes form an 8 x 4 grid and each owns two 4 x 4 blocks per dimension (rows
-// ty*4 + {0,32}, columns tx*4 + {0,16}), so every fragment read is one shared-memory
-// wavefront and every float4 store row is 64 contiguous bytes per 4 lanes.
+// 128 x 256 x 16 block tile, 256 threads as 2 x 4 warps of 64 x 64; inside a warp the
+// lanes form an 8 x 4 grid and each owns 8 rows x 16 columns: rows ty*4 + {0,32} + {0..3},
+// columns tx*4 + {0,16,32,48} + {0..3}.  Every fragment read is one shared-memory
+// wavefront and every float4 store row is 64 contiguous bytes per 4 lanes.  The packed
+// FMAs pair columns: one duplicated A value per row serves 8 of them, so the register
+// moves that build the (a, a) pairs cost 1 per 8 packed FMAs (1 per 4 with 8 columns per
+// thread: 58.6 against 63.0 TFLOP/s at 8192^3).
 // Two instantiations: EDGE = false for tiles wholly inside M x N with K a multiple of 16
 // and aligned operands (no predicates, running pointers), EDGE = true for everything
 // else (predicated, zero-filled loads).  The host launches the interior tiles and the
-// L-shaped edge region separately.
-constexpr int W_BM = 128, W_BN = 128, W_BK = 16;
-// Resident blocks per SM the kernel is compiled for.  With the packed FMAs the 8 x 8 block
-// needs ~150 registers: one block of 8 warps per SM without spills measured faster on
-// GB300 (54.7 TFLOP/s at 4096^3) than two blocks capped at 128 registers (49.8, spilling).
-int g_warptile_min_blocks = 1;
+// L-shaped edge region separately.  One block per SM (~254 registers, 48.6 KiB of
+// dynamic shared memory).
+constexpr int W_BM = 128, W_BN = 256, W_BK = 16;
+constexpr int W_AS_LD = W_BM + 4;  // padded row of the k-major A tile
+constexpr int W_SMEM_BYTES = (2 * W_BK * W_AS_LD + 2 * W_BK * W_BN) * 4;
 
 // A last, partial wave of interior tiles leaves SMs idle for a whole tile time.  Its tiles
 // can instead run cut along K into `rs` pieces (K slices of one tile, summed in fixed order
@@ -282,60 +285,50 @@ __device__ __forceinline__ void map_tile(const TileMap& t, int pid, int& mt, int
     }
 }
 
-template <int MIN_BLOCKS, bool EDGE>
-__global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
-ffma_warptile_kernel(F32Args p, int64_t k_per_split, TileMap tmap, float* ws, int vec_in, int vec_out)
+// Sizes and leading dimensions come as 32-bit scalars (the host keeps them below 2^31),
+// widened where addresses are formed: with 64-bit leading dimensions the same body
+// measured 20 % slower (50.2 against 63.0 TFLOP/s at 8192^3; the address arithmetic of
+// the loads can no longer stay in 32 bits).
+template <bool EDGE>
+__global__ void __launch_bounds__(kThreads, 1)
+ffma_warptile_kernel(const float* __restrict__ A, int lda_, const float* __restrict__ B, int ldb_,
+                     float* __restrict__ C, int ldc_, int M, int N, int K, int k_per_split, TileMap tmap,
+                     float* __restrict__ ws, int vec_in, int vec_out)
 {
-    constexpr int AS_LD = W_BM + 4;
-    __shared__ __align__(16) float As[2][W_BK][AS_LD];
-    __shared__ __align__(16) float Bs[2][W_BK][W_BN];
+    const int64_t lda = lda_, ldb = ldb_, ldc = ldc_;
+    extern __shared__ __align__(16) float w_smem[];
+    float (*As)[W_BK][W_AS_LD] = reinterpret_cast<float (*)[W_BK][W_AS_LD]>(w_smem);
+    float (*Bs)[W_BK][W_BN] = reinterpret_cast<float (*)[W_BK][W_BN]>(w_smem + 2 * W_BK * W_AS_LD);
 
     const int tid = threadIdx.x;
     int mt, nt;
     map_tile(tmap, tmap.first + blockIdx.x, mt, nt);
     const int64_t m0 = (int64_t)mt * W_BM, n0 = (int64_t)nt * W_BN;
-    const int64_t kbeg = (int64_t)blockIdx.z * k_per_split;
-    const int64_t kend = min(p.K, kbeg + k_per_split);
-
-    // output rows: C, or a split-K partial (a full M x N slice, or one BM x BN tile);
-    // element (gm, gn) lives at out[(gm - row0) * ldo + (gn - col0)]
-    float* out;
-    int64_t ldo, row0 = 0, col0 = 0;
-    if (tmap.compact) {
-        out = ws + ((int64_t)blockIdx.z * gridDim.x + blockIdx.x) * (W_BM * W_BN);
-        ldo = W_BN;
-        row0 = m0;
-        col0 = n0;
-    } else if (gridDim.z > 1) {
-        out = ws + (int64_t)blockIdx.z * p.M * p.N;
-        ldo = p.N;
-    } else {
-        out = p.C;
-        ldo = p.ldc;
-    }
+    const int kbeg = (int)blockIdx.z * k_per_split;  // < K
+    const int kend = (int)min((int64_t)K, (int64_t)kbeg + k_per_split);
 
     // global -> register staging: A float4s at (row a_row, k a_kq) and (a_row, a_kq + 8);
-    // B float4s at (k b_k, cols b_nq..+3) and (b_k + 8, b_nq..+3)
+    // B float4s at (k b_k + 4 h, cols b_nq..+3), h = 0..3
     const int a_row = tid % W_BM, a_kq = (tid / W_BM) * 4;
-    const int b_k = tid / 32, b_nq = (tid % 32) * 4;
-    const bool a_ok = !EDGE || (m0 + a_row) < p.M;
-    const float* a_cur = p.A + (a_ok ? (m0 + a_row) : 0) * p.lda + kbeg + a_kq;
-    const float* b_cur = p.B + (kbeg + b_k) * p.ldb + n0 + b_nq;
-    const int64_t b_half = 8 * p.ldb;
+    const int b_k = tid / 64, b_nq = (tid % 64) * 4;
+    const bool a_ok = !EDGE || (m0 + a_row) < M;
+    const float* a_cur = A + (a_ok ? (m0 + a_row) : 0) * lda + kbeg + a_kq;
+    const float* b_cur = B + (int64_t)(kbeg + b_k) * ldb + n0 + b_nq;
+    const int64_t b_step = 4 * ldb;
 
-    float4 ra[2], rb[2];
-    int64_t k_next = kbeg;  // k of the tile the next load() fetches
+    float4 ra[2], rb[4];
+    int k_next = kbeg;  // k of the tile the next load() fetches
     auto load = [&]() {
         if constexpr (!EDGE) {
             ra[0] = __ldg(reinterpret_cast<const float4*>(a_cur));
             ra[1] = __ldg(reinterpret_cast<const float4*>(a_cur + 8));
-            rb[0] = __ldg(reinterpret_cast<const float4*>(b_cur));
-            rb[1] = __ldg(reinterpret_cast<const float4*>(b_cur + b_half));
+#pragma unroll
+            for (int h = 0; h < 4; ++h) rb[h] = __ldg(reinterpret_cast<const float4*>(b_cur + h * b_step));
         } else {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                const int64_t gk = k_next + a_kq + h * 8;
+                const int gk = k_next + a_kq + h * 8;
                 if (a_ok) {
                     const float* src = a_cur + h * 8;
                     if (vec_in && gk + 3 < kend) {
@@ -348,18 +341,21 @@ ffma_warptile_kernel(F32Args p, int64_t k_per_split, TileMap tmap, float* ws, in
                     }
                 }
                 ra[h] = v;
-                v = make_float4(0.f, 0.f, 0.f, 0.f);
-                const int64_t bk = k_next + b_k + h * 8;
+            }
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                const int bk = k_next + b_k + h * 4;
                 const int64_t gn = n0 + b_nq;
                 if (bk < kend) {
-                    const float* src = b_cur + h * b_half;
-                    if (vec_in && gn + 3 < p.N) {
+                    const float* src = b_cur + h * b_step;
+                    if (vec_in && gn + 3 < N) {
                         v = __ldg(reinterpret_cast<const float4*>(src));
                     } else {
-                        if (gn + 0 < p.N) v.x = __ldg(src + 0);
-                        if (gn + 1 < p.N) v.y = __ldg(src + 1);
-                        if (gn + 2 < p.N) v.z = __ldg(src + 2);
-                        if (gn + 3 < p.N) v.w = __ldg(src + 3);
+                        if (gn + 0 < N) v.x = __ldg(src + 0);
+                        if (gn + 1 < N) v.y = __ldg(src + 1);
+                        if (gn + 2 < N) v.z = __ldg(src + 2);
+                        if (gn + 3 < N) v.w = __ldg(src + 3);
                     }
                 }
                 rb[h] = v;
@@ -367,7 +363,7 @@ ffma_warptile_kernel(F32Args p, int64_t k_per_split, TileMap tmap, float* ws, in
             k_next += W_BK;
         }
         a_cur += W_BK;
-        b_cur += 2 * b_half;
+        b_cur += 4 * b_step;
     };
     auto store = [&](int buf) {
 #pragma unroll
@@ -377,25 +373,27 @@ ffma_warptile_kernel(F32Args p, int64_t k_per_split, TileMap tmap, float* ws, in
             As[buf][a_kq + h * 8 + 1][a_row] = ra[h].y;
             As[buf][a_kq + h * 8 + 2][a_row] = ra[h].z;
             As[buf][a_kq + h * 8 + 3][a_row] = ra[h].w;
-            *reinterpret_cast<float4*>(&Bs[buf][b_k + h * 8][b_nq]) = rb[h];
         }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) *reinterpret_cast<float4*>(&Bs[buf][b_k + h * 4][b_nq]) = rb[h];
     };
 
     const int warp = tid / 32, lane = tid % 32;
     const int wm = warp / 4, wn = warp % 4;  // 2 x 4 warps
     const int ty = lane / 4, tx = lane % 4;  // 8 x 4 lanes
     const int a_frag = wm * 64 + ty * 4;     // rows a_frag + {0..3}, a_frag + 32 + {0..3}
-    const int b_frag = wn * 32 + tx * 4;     // cols b_frag + {0..3}, b_frag + 16 + {0..3}
+    const int b_frag = wn * 64 + tx * 4;     // cols b_frag + 16 h + {0..3}, h = 0..3
 
-    // acc[i][jj] holds columns (2jj, 2jj+1) of accumulator row i: the outer product runs
-    // as packed fp32 FMAs (fma.rn.f32x2, two independent round-to-nearest FMAs per issue)
-    float2 acc[8][4];
+    // acc[i][jj] holds columns (2jj, 2jj+1) of this thread's 16 in accumulator row i: the
+    // outer product runs as packed fp32 FMAs (fma.rn.f32x2, two independent
+    // round-to-nearest FMAs per issue)
+    float2 acc[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
+        for (int j = 0; j < 8; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-    const int ktiles = (kend > kbeg) ? (int)((kend - kbeg + W_BK - 1) / W_BK) : 0;
+    const int ktiles = (kend > kbeg) ? (kend - kbeg + W_BK - 1) / W_BK : 0;
     if (ktiles > 0) {
         load();
         store(0);
@@ -408,37 +406,57 @@ ffma_warptile_kernel(F32Args p, int64_t k_per_split, TileMap tmap, float* ws, in
         for (int k = 0; k < W_BK; ++k) {
             const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][a_frag]);
             const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][a_frag + 32]);
-            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][b_frag]);
-            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][b_frag + 16]);
+            float2 bp[8];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float4 b = *reinterpret_cast<const float4*>(&Bs[buf][k][b_frag + 16 * h]);
+                bp[2 * h] = make_float2(b.x, b.y);
+                bp[2 * h + 1] = make_float2(b.z, b.w);
+            }
             const float af[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
-                                  make_float2(b1.z, b1.w)};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float2 ai = make_float2(af[i], af[i]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(ai, bp[j], acc[i][j]);
+                for (int j = 0; j < 8; ++j) acc[i][j] = __ffma2_rn(ai, bp[j], acc[i][j]);
             }
         }
         if (kt + 1 < ktiles) store(buf ^ 1);
         __syncthreads();
     }
 
+    // output rows: C, or a split-K partial (a full M x N slice, or one BM x BN tile);
+    // element (gm, gn) lives at out[(gm - row0) * ldo + (gn - col0)].  (Worked out only
+    // now, so that none of it stays live in registers through the main loop.)
+    float* out;
+    int64_t ldo, row0 = 0, col0 = 0;
+    if (tmap.compact) {
+        out = ws + ((int64_t)blockIdx.z * gridDim.x + blockIdx.x) * (W_BM * W_BN);
+        ldo = W_BN;
+        row0 = m0;
+        col0 = n0;
+    } else if (gridDim.z > 1) {
+        out = ws + (int64_t)blockIdx.z * M * N;
+        ldo = N;
+    } else {
+        out = C;
+        ldo = ldc;
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t gm = m0 + a_frag + (i / 4) * 32 + (i % 4);
-        if (EDGE && gm >= p.M) continue;
+        if (EDGE && gm >= M) continue;
         float* row = out + (gm - row0) * ldo - col0;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 4; ++h) {
             const int64_t gn = n0 + b_frag + h * 16;
             const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y};
-            if ((vec_out || tmap.compact) && (!EDGE || gn + 3 < p.N)) {
+            if ((vec_out || tmap.compact) && (!EDGE || gn + 3 < N)) {
                 *reinterpret_cast<float4*>(row + gn) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (gn + j < p.N) row[gn + j] = v[j];
+                    if (gn + j < N) row[gn + j] = v[j];
             }
         }
     }
@@ -543,25 +561,42 @@ cudaError_t launch_variant(const F32Args& a, int split, float* ws, cudaStream_t 
     return launch_splitk_reduce(ws, nsplit, a.M, a.N, a.C, a.ldc, 0, stream);
 }
 
-template <int MIN_BLOCKS>
-cudaError_t launch_warptile_occ(const F32Args& a, int64_t kps, int nsplit, float* ws, int vec_in, int vec_out,
-                                int64_t remainder_slots, cudaStream_t stream, int* launches)
+cudaError_t launch_warptile(const F32Args& a, int split, float* ws, int remainder_split, int num_sms,
+                            cudaStream_t stream, int* launches)
 {
-    const int m_tiles = (int)((a.M + W_BM - 1) / W_BM), n_tiles = (int)((a.N + W_BN - 1) / W_BN);
+    const int64_t m_tiles64 = (a.M + W_BM - 1) / W_BM, n_tiles64 = (a.N + W_BN - 1) / W_BN;
+    // the kernel takes sizes and leading dimensions as 32-bit values
+    if (m_tiles64 * n_tiles64 > 0x7fffffffLL || a.M > 0x7fffffffLL || a.N > 0x7fffffffLL ||
+        a.K > 0x7fffffffLL - W_BK || a.lda > 0x7fffffffLL || a.ldb > 0x7fffffffLL || a.ldc > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    int64_t kps = (a.K + split - 1) / split;
+    kps = (kps + W_BK - 1) / W_BK * W_BK;
+    const int nsplit = (int)((a.K + kps - 1) / kps);
+    const int vec_in = ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15) == 0 &&
+                       a.lda % 4 == 0 && a.ldb % 4 == 0;
+    int vec_out;
+    if (nsplit > 1)
+        vec_out = (a.N % 4 == 0);
+    else
+        vec_out = (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0;
+    for (auto kern : {ffma_warptile_kernel<false>, ffma_warptile_kernel<true>})
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, W_SMEM_BYTES) != cudaSuccess)
+            return cudaGetLastError();
+    const int m_tiles = (int)m_tiles64, n_tiles = (int)n_tiles64;
     const int m_full = (int)(a.M / W_BM), n_full = (int)(a.N / W_BN);
     const bool fast_ok = vec_in && (a.K % W_BK == 0);
     const int interior = fast_ok ? m_full * n_full : 0;
     const int64_t edge = (int64_t)m_tiles * n_tiles - interior;
     if (interior > 0) {
         // whole waves as usual; the tiles of a last, partial wave (if any) are cut along
-        // K so that they fill the GPU's `remainder_slots` block slots (remainder_plan)
+        // K so that they fill the GPU's block slots (one per SM; remainder_plan)
         int rem = 0, rs = 1;
-        if (remainder_slots > 0) remainder_plan(interior, remainder_slots, a.K, &rem, &rs);
+        if (nsplit == 1 && remainder_split) remainder_plan(interior, num_sms, a.K, &rem, &rs);
         const int main_tiles = interior - rem;
         TileMap t{0, m_full, n_full, m_tiles, n_tiles};
         if (main_tiles > 0) {
-            ffma_warptile_kernel<MIN_BLOCKS, false><<<dim3(main_tiles, 1, nsplit), kThreads, 0, stream>>>(
-                a, kps, t, ws, vec_in, vec_out);
+            ffma_warptile_kernel<false><<<dim3(main_tiles, 1, nsplit), kThreads, W_SMEM_BYTES, stream>>>(
+                a.A, (int)a.lda, a.B, (int)a.ldb, a.C, (int)a.ldc, (int)a.M, (int)a.N, (int)a.K, (int)kps, t, ws, vec_in, vec_out);
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return e;
             *launches += 1;
@@ -573,8 +608,8 @@ cudaError_t launch_warptile_occ(const F32Args& a, int64_t kps, int nsplit, float
             TileMap tr = t;
             tr.first = main_tiles;
             tr.compact = 1;
-            ffma_warptile_kernel<MIN_BLOCKS, false><<<dim3(rem, 1, rsplit), kThreads, 0, stream>>>(
-                a, rkps, tr, ws, vec_in, vec_out);
+            ffma_warptile_kernel<false><<<dim3(rem, 1, rsplit), kThreads, W_SMEM_BYTES, stream>>>(
+                a.A, (int)a.lda, a.B, (int)a.ldb, a.C, (int)a.ldc, (int)a.M, (int)a.N, (int)a.K, (int)rkps, tr, ws, vec_in, vec_out);
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return e;
             int64_t blocks = (int64_t)rem * W_BM * W_BN / 4 / 256;
@@ -587,35 +622,13 @@ cudaError_t launch_warptile_occ(const F32Args& a, int64_t kps, int nsplit, float
     }
     if (edge > 0) {
         TileMap t = fast_ok ? TileMap{1, m_full, n_full, m_tiles, n_tiles} : TileMap{0, m_tiles, n_tiles, m_tiles, n_tiles};
-        ffma_warptile_kernel<MIN_BLOCKS, true><<<dim3((unsigned)edge, 1, nsplit), kThreads, 0, stream>>>(
-            a, kps, t, ws, vec_in, vec_out);
+        ffma_warptile_kernel<true><<<dim3((unsigned)edge, 1, nsplit), kThreads, W_SMEM_BYTES, stream>>>(
+            a.A, (int)a.lda, a.B, (int)a.ldb, a.C, (int)a.ldc, (int)a.M, (int)a.N, (int)a.K, (int)kps, t, ws, vec_in, vec_out);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         *launches += 1;
     }
-    return cudaSuccess;
-}
-
-cudaError_t launch_warptile(const F32Args& a, int split, float* ws, int remainder_split, int num_sms,
-                            cudaStream_t stream, int* launches)
-{
-    const int64_t m_tiles = (a.M + W_BM - 1) / W_BM, n_tiles = (a.N + W_BN - 1) / W_BN;
-    if (m_tiles * n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    int64_t kps = (a.K + split - 1) / split;
-    kps = (kps + W_BK - 1) / W_BK * W_BK;
-    const int nsplit = (int)((a.K + kps - 1) / kps);
-    const int vec_in = ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15) == 0 &&
-                       a.lda % 4 == 0 && a.ldb % 4 == 0;
-    int vec_out;
-    if (nsplit > 1)
-        vec_out = (a.N % 4 == 0);
-    else
-        vec_out = (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0;
-    const int64_t slots = (nsplit == 1 && remainder_split) ? (int64_t)num_sms * g_warptile_min_blocks : 0;
-    cudaError_t e = (g_warptile_min_blocks == 1)
-                        ? launch_warptile_occ<1>(a, kps, nsplit, ws, vec_in, vec_out, slots, stream, launches)
-                        : launch_warptile_occ<2>(a, kps, nsplit, ws, vec_in, vec_out, slots, stream, launches);
-    if (e != cudaSuccess || nsplit == 1) return e;
+    if (nsplit == 1) return cudaSuccess;
     *launches += 1;
     return launch_splitk_reduce(ws, nsplit, a.M, a.N, a.C, a.ldc, 0, stream);
 }
@@ -630,13 +643,13 @@ int64_t ffma_remainder_workspace(const F32Args& a, int variant, int split, int n
                         a.lda % 4 == 0 && a.ldb % 4 == 0;
     if (!vec_in || a.K % W_BK) return 0;
     int rem = 0, rs = 1;
-    remainder_plan((a.M / W_BM) * (a.N / W_BN), (int64_t)num_sms * g_warptile_min_blocks, a.K, &rem, &rs);
+    remainder_plan((a.M / W_BM) * (a.N / W_BN), num_sms, a.K, &rem, &rs);
     return (int64_t)rem * rs * W_BM * W_BN;
 }
 
 int ffma_auto_split(const F32Args& a, int variant, int num_sms)
 {
-    const int BM = (variant == 2) ? 64 : 128, BN = 128, BK = 16;
+    const int BM = (variant == 2) ? 64 : W_BM, BN = (variant == 2) ? 128 : W_BN, BK = 16;
     const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
     const int64_t capacity = (int64_t)num_sms * 2;  // two resident blocks per SM
     if (tiles >= capacity) return 1;

@@ -41,7 +41,7 @@ struct F32Args {
     int64_t ldc;
 };
 
-// fp32 tiled FFMA GEMM (128x128 or 32x128 block tiles), optional split-K.
+// fp32 tiled FFMA GEMM (128x256 or 64x128 block tiles), optional split-K.
 // With split > 1 the partial products go to `workspace` ([split][M][N], ld = N) and a
 // fixed-order reduction writes C.  Returns a cudaError_t.
 cudaError_t launch_ffma_tiled(const F32Args& a, int variant, int split, float* workspace,
@@ -66,7 +66,7 @@ cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t 
 // The driver's cuTensorMapEncodeTiled (looked up once), or nullptr if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
-// Workspace floats the 128x128 FFMA path needs to split the tiles of a last, partial wave
+// Workspace floats the 128x256 FFMA path needs to split the tiles of a last, partial wave
 // along K (0 when it does not apply).
 int64_t ffma_remainder_workspace(const F32Args& a, int variant, int split, int num_sms);
 

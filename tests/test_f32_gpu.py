@@ -3,7 +3,7 @@
 Tolerances (max |C - C_ref| over the compared entries):
   * integer-valued inputs in [-4, 4]: exact (every partial sum is an integer below 2^24);
   * uniform[-1, 1] inputs: 1e-5 * sqrt(K).
-Kernels: the 128x128 and 64x128 tiled FFMA kernels (with and without split-K) and the two
+Kernels: the 128x256 and 64x128 tiled FFMA kernels (with and without split-K) and the two
 skinny kernels (B streamed through registers, or through a TMA ring in shared memory),
 each forced on shapes with ragged tails, padded leading dimensions and guard bands
 around C.
@@ -169,17 +169,17 @@ def last_wave_plan(interior, slots, K):
     return (0, 1) if best_t > 0.85 else (rem, best_rs)
 
 
-@pytest.mark.parametrize("M,N", [(1664, 1664), (1701, 1669)])
+@pytest.mark.parametrize("M,N", [(1664, 3328), (1701, 3341)])
 def test_last_wave_tiles_split_along_K(lib, M, N):
-    # 13 x 13 = 169 interior 128 x 128 tiles: on 152 SMs the 17 tiles of the last wave run
+    # 13 x 13 = 169 interior 128 x 256 tiles: on 152 SMs the 17 tiles of the last wave run
     # cut into K slices whose partial tiles are summed in a separate fixed-order pass
     K = 2048
     slots = torch.cuda.get_device_properties(0).multi_processor_count
-    rem, rs = last_wave_plan((M // 128) * (N // 128), slots, K)
+    rem, rs = last_wave_plan((M // 128) * (N // 256), slots, K)
     Ai, Bi = si.integer_copy(M, N, K, seed=M)
     n0 = lib.launch_count()
     got = run_padded(lib, Ai, Bi, pad_b=-N % 4, pad_c=4)  # rows of B 16-byte aligned: vector loads
-    edge = (M % 128 != 0) or (N % 128 != 0)
+    edge = (M % 128 != 0) or (N % 256 != 0)
     assert lib.launch_count() - n0 == 1 + (2 if rem else 0) + (1 if edge else 0)
     assert np.array_equal(got, ref_of(Ai, Bi))
     A, B = si.gemm_operands(M, N, K, seed=M + 1)
