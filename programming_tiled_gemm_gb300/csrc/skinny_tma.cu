@@ -49,7 +49,8 @@ struct StCfg {
 
 struct StParams {
     F32Args a;
-    int64_t k_per_split;
+    int k_per_split;  // (sizes in 32 bits: the host keeps K and lda below 2^31)
+    int K, lda;
     int nsplit;
     int col_blocks;
     int num_items;  // col_blocks * nsplit
@@ -104,10 +105,10 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
         bool ok = true;
         for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
             const int cb = item % p.col_blocks, sp = item / p.col_blocks;
-            const int64_t kbeg = (int64_t)sp * p.k_per_split;
-            const int64_t kend = min(a.K, kbeg + p.k_per_split);
+            const int kbeg = sp * p.k_per_split;
+            const int kend = (int)min((int64_t)p.K, (int64_t)kbeg + p.k_per_split);
             const int col0 = cb * ST_COLS;
-            for (int64_t k0 = kbeg; k0 < kend; k0 += ST_KROWS) {
+            for (int k0 = kbeg; k0 < kend; k0 += ST_KROWS) {
                 // this stage's A[m][k0 .. k0+7] into registers first: its L2 latency overlaps
                 // the wait for a free stage (zero past M and past this slice's K)
                 float av[ST_KROWS * MR / 32];
@@ -115,8 +116,8 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
                 for (int i = 0; i < ST_KROWS * MR / 32; ++i) {
                     const int e = lane + 32 * i;
                     const int kk = e % ST_KROWS, m = e / ST_KROWS;
-                    const int64_t gk = k0 + kk;
-                    av[i] = (m < a.M && gk < kend) ? __ldg(a.A + (int64_t)m * a.lda + gk) : 0.f;
+                    const int gk = k0 + kk;
+                    av[i] = (m < a.M && gk < kend) ? __ldg(a.A + (int64_t)m * p.lda + gk) : 0.f;
                 }
                 bool got = (lane == 0) ? mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.limit_ns, abort_flag)
                                        : true;
@@ -183,8 +184,8 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
         }
         for (int item = item_first; item < p.num_items; item += gridDim.x) {
             const int cb = item % p.col_blocks, sp = item / p.col_blocks;
-            const int64_t kbeg = (int64_t)sp * p.k_per_split;
-            const int64_t kend = min(a.K, kbeg + p.k_per_split);
+            const int kbeg = sp * p.k_per_split;
+            const int kend = (int)min((int64_t)p.K, (int64_t)kbeg + p.k_per_split);
             // column offset inside the stage: box j holds columns 256j .. 256j+255, stored
             // [k][256] per box
             const int box = ct / 64, in_box = (ct % 64) * 4;
@@ -192,7 +193,7 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
 #pragma unroll
             for (int m = 0; m < RT; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
             bool ok = true;
-            for (int64_t k0 = kbeg; k0 < kend; k0 += ST_KROWS) {
+            for (int k0 = kbeg; k0 < kend; k0 += ST_KROWS) {
                 bool got = mbar_wait(smem_u32(&full_bar[stage]), phase, p.limit_ns, abort_flag);
                 got = __all_sync(0xffffffffu, got);
                 if (!got) {
@@ -279,7 +280,9 @@ cudaError_t launch_mr_tma(const F32Args& a, int split, float* ws, int num_sms, i
     p.a = a;
     int64_t kps = (a.K + split - 1) / split;
     kps = (kps + ST_KROWS - 1) / ST_KROWS * ST_KROWS;  // slices start on a stage boundary
-    p.k_per_split = kps;
+    p.k_per_split = (int)kps;
+    p.K = (int)a.K;
+    p.lda = (int)a.lda;
     p.nsplit = (int)((a.K + kps - 1) / kps);
     p.col_blocks = (int)((a.N + StCfg<MR, COLW, MSPLIT>::COLS - 1) / StCfg<MR, COLW, MSPLIT>::COLS);
     const int64_t items = (int64_t)p.col_blocks * p.nsplit;
@@ -313,7 +316,8 @@ cudaError_t launch_mr_tma(const F32Args& a, int split, float* ws, int num_sms, i
 bool skinny_tma_supported(const F32Args& a)
 {
     // TMA: 16-byte aligned base, row stride a multiple of 16 bytes
-    return a.M <= 32 && (reinterpret_cast<uintptr_t>(a.B) & 15) == 0 && a.ldb % 4 == 0 && a.K < (1ll << 31) &&
+    return a.M <= 32 && (reinterpret_cast<uintptr_t>(a.B) & 15) == 0 && a.ldb % 4 == 0 && a.K < (1ll << 31) - 64 &&
+           a.lda < (1ll << 31) &&
            a.N < (1ll << 31);
 }
 
