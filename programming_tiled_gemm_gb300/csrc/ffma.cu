@@ -29,11 +29,23 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kGroupM = 8;  // output-tile rows per raster group (L2 reuse of B columns)
 
+// Sizes and leading dimensions arrive as 32-bit values (the host keeps them below 2^31),
+// so that the compiler can keep the load-address arithmetic in 32 bits; they are widened
+// into `p` only where addresses are formed.
 template <int BM, int BN, int BK, int TM, int TN, bool VEC>
 __global__ void __launch_bounds__(kThreads, 2)
-ffma_tiled_kernel(F32Args p, int64_t k_per_split, int m_tiles, int n_tiles, float* ws,
+ffma_tiled_kernel(const float* __restrict__ A, int lda, const float* __restrict__ B, int ldb, float* __restrict__ C,
+                  int ldc, int M, int N, int K, int k_per_split, int m_tiles, int n_tiles, float* __restrict__ ws,
                   int vec_out)
 {
+    const struct {
+        const float* A;
+        int64_t lda;
+        const float* B;
+        int64_t ldb;
+        float* C;
+        int64_t ldc, M, N, K;
+    } p = {A, lda, B, ldb, C, ldc, M, N, K};
     constexpr int TY = BM / TM;  // thread rows
     constexpr int TX = BN / TN;  // thread columns
     static_assert(TY * TX == kThreads, "tile/thread mismatch");
@@ -535,7 +547,10 @@ template <int BM, int BN, int BK, int TM, int TN>
 cudaError_t launch_variant(const F32Args& a, int split, float* ws, cudaStream_t stream, int* launches)
 {
     const int64_t m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + BN - 1) / BN;
-    if (m_tiles * n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // the kernel takes sizes and leading dimensions as 32-bit values
+    if (m_tiles * n_tiles > 0x7fffffffLL || a.M > 0x7fffffffLL || a.N > 0x7fffffffLL || a.K > 0x7fffffffLL - BK ||
+        a.lda > 0x7fffffffLL || a.ldb > 0x7fffffffLL || a.ldc > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
     int64_t kps = (a.K + split - 1) / split;
     kps = (kps + BK - 1) / BK * BK;  // every split but the last starts on a tile boundary
     const int nsplit = (int)((a.K + kps - 1) / kps);
@@ -549,10 +564,12 @@ cudaError_t launch_variant(const F32Args& a, int split, float* ws, cudaStream_t 
     dim3 grid((unsigned)(m_tiles * n_tiles), 1, (unsigned)nsplit);
     if (vec_in)
         ffma_tiled_kernel<BM, BN, BK, TM, TN, true><<<grid, kThreads, 0, stream>>>(
-            a, kps, (int)m_tiles, (int)n_tiles, ws, vec_out);
+            a.A, (int)a.lda, a.B, (int)a.ldb, a.C, (int)a.ldc, (int)a.M, (int)a.N, (int)a.K, (int)kps, (int)m_tiles,
+            (int)n_tiles, ws, vec_out);
     else
         ffma_tiled_kernel<BM, BN, BK, TM, TN, false><<<grid, kThreads, 0, stream>>>(
-            a, kps, (int)m_tiles, (int)n_tiles, ws, vec_out);
+            a.A, (int)a.lda, a.B, (int)a.ldb, a.C, (int)a.ldc, (int)a.M, (int)a.N, (int)a.K, (int)kps, (int)m_tiles,
+            (int)n_tiles, ws, vec_out);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     *launches += 1;
