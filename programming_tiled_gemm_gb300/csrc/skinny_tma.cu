@@ -327,7 +327,7 @@ static int64_t st_cols_for(int64_t M) { return M <= 16 ? StCfg<16, 8, 1>::COLS :
 int skinny_tma_auto_split(const F32Args& a, int num_sms)
 {
     // the fewest K slices whose (column block, slice) items fill the persistent grid's
-    // waves to at least 92 %; more slices only add partial-sum traffic
+    // waves to at least 97 %; more slices only add partial-sum traffic
     const int64_t cols = st_cols_for(a.M);
     const int64_t cbs = (a.N + cols - 1) / cols;
     int64_t max_s = (a.K + 16 * ST_KROWS - 1) / (16 * ST_KROWS);  // at least 16 stages per slice
@@ -339,7 +339,7 @@ int skinny_tma_auto_split(const F32Args& a, int num_sms)
         const int64_t items = cbs * s;
         const int64_t waves = (items + num_sms - 1) / num_sms;
         const double eff = (double)items / (double)(waves * num_sms);
-        if (eff >= 0.92) return (int)s;
+        if (eff >= 0.97) return (int)s;
         if (eff > best_eff + 1e-9) {
             best_eff = eff;
             best = s;
