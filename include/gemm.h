@@ -182,7 +182,9 @@ int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t 
  * partial sums that are added in fp32 round-to-nearest, in order.  Deterministic.
  * Asynchronous on `stream`.  Two launches: one stages the input and the weights in the
  * handle's workspace (grown on demand, about the size of x plus the size of w times
- * (k[3] + 2S - 2) / k[3], S from GEMM_OPT_CONV_STACK), one computes y.
+ * (k[3] + 2S - 2) / k[3], S from GEMM_OPT_CONV_STACK), one computes y (a programmatic
+ * dependent launch: it sets up while the first runs and waits for it before reading the
+ * workspace).
  * x, w and y must be 16-byte aligned (GEMM_ERR_ALIGNMENT).
  * GEMM_ERR_INVALID_ARG for bad extents, pointers or dtype (GEMM_BF16 or GEMM_F16 only);
  * GEMM_ERR_UNSUPPORTED unless C_in % 16 == 0, C_out % 16 == 0, S * C_out <= 256,

@@ -109,6 +109,8 @@ __device__ __forceinline__ void ct_record_error(int* status, int code, volatile 
 __global__ void __launch_bounds__(256)
 conv_tc_prepare_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w, ConvTcParams p, uint4* xp, uint4* wp)
 {
+    // the conv kernel may start its set-up now; it waits for this grid before reading xp / wp
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int cg = p.cin / 8;
     const int mS = p.I[3] / p.S;
     const int nblk = p.I[0] * cg * p.S;
@@ -188,6 +190,9 @@ __global__ void __launch_bounds__(CT_THREADS, 1) conv4d_tc_kernel(ConvTcParams p
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
+            // launched as a programmatic dependent of the staging kernel: its writes to the
+            // workspace are complete and visible once this returns
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             uint32_t issued_mask = 0, last_parity = 0;
             const int64_t row_bytes = (int64_t)(p.I[3] / p.S) * 16;
             const int64_t blk_stride = (int64_t)p.xp_rows * row_bytes;  // one (i0, g, phase) block
@@ -519,8 +524,19 @@ int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void
     const int smem = p.nstages_ring * p.stage_bytes + 1024 /*barriers*/ + 1024 /*alignment slack*/;
     if (cudaFuncSetAttribute(conv4d_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GEMM_ERR_CUDA;
-    conv4d_tc_kernel<<<(unsigned)(p.tiles_per_p0 * p.P[0]), CT_THREADS, smem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+    // programmatic dependent launch: the CTAs set up their barriers and TMEM while the
+    // staging kernel still runs; the producer waits for it before its first copy
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.tiles_per_p0 * p.P[0]));
+    cfg.blockDim = dim3(CT_THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, conv4d_tc_kernel, p) != cudaSuccess) return GEMM_ERR_CUDA;
     *launches += 1;
     return GEMM_OK;
 }
