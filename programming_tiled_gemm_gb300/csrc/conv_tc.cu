@@ -104,40 +104,50 @@ __device__ __forceinline__ void ct_record_error(int* status, int code, volatile 
 //                                (zero for row >= I1 * I2; rows 0 .. xp_rows - 1)
 //   wp[trip][g][j][o]          = w[o][r0][r1][r2][R3 + S - 2 - j][8 g .. 8 g + 7]
 //                                (zero when that r3 is outside 0 .. R3 - 1)
-//   grid.y < I0 * C_in/8 * S: one (i0, g, phase) block of xp per y, rows x entries along x;
-//   the rest of grid.y: one filter triple's weights per y.
+// One flat index over four segments, one 16-byte chunk per thread: the input in its own
+// order (coalesced reads, scattered writes), the input's zero rows, the weights in their
+// own order, the zero weight slices.  The chunk counts fit 31 bits (checked by the plan).
 __global__ void __launch_bounds__(256)
 conv_tc_prepare_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w, ConvTcParams p, uint4* xp, uint4* wp)
 {
     // the conv kernel may start its set-up now; it waits for this grid before reading xp / wp
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int cg = p.cin / 8;
-    const int mS = p.I[3] / p.S;
-    const int nblk = p.I[0] * cg * p.S;
-    const int by = blockIdx.y;
-    if (by < nblk) {
-        const int ph = by % p.S, g = (by / p.S) % cg, i0 = by / (p.S * cg);
-        const int plane_rows = p.I[1] * p.I[2];
-        const int n = p.xp_rows * mS;
-        uint4* dst = xp + (int64_t)by * n;
-        const uint4* src = x + (int64_t)i0 * plane_rows * p.I[3] * cg + g;
-        for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
-            const int row = e / mS, m = e - row * mS;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (row < plane_rows) v = src[((int64_t)row * p.I[3] + ph + p.S * m) * cg];
-            dst[e] = v;
-        }
-    } else {
-        const int trip = by - nblk;
-        const int trips = p.R[0] * p.R[1] * p.R[2];
-        const int n = cg * p.nslices * p.cout;  // (g, j, o) of this triple
-        uint4* dst = wp + (int64_t)trip * n;
-        for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
-            const int o = e % p.cout, j = (e / p.cout) % p.nslices, g = e / (p.cout * p.nslices);
-            const int r3 = p.R[3] + p.S - 2 - j;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r3 >= 0 && r3 < p.R[3]) v = w[(((int64_t)o * trips + trip) * p.R[3] + r3) * cg + g];
-            dst[e] = v;
+    const int cg = p.cin / 8, S = p.S, mS = p.I[3] / S;
+    const int plane_rows = p.I[1] * p.I[2];
+    const int trips = p.R[0] * p.R[1] * p.R[2];
+    const int n_x = p.I[0] * plane_rows * p.I[3] * cg;
+    const int tail = p.xp_rows - plane_rows;
+    const int n_xz = p.I[0] * cg * S * tail * mS;
+    const int n_w = p.cout * trips * p.R[3] * cg;
+    const int zs = 2 * S - 2;  // zero slices per (trip, g)
+    const int n_wz = trips * cg * zs * p.cout;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n_x + n_xz + n_w + n_wz; e += gridDim.x * blockDim.x) {
+        if (e < n_x) {
+            const int g = e % cg, pos = e / cg;
+            const int i3 = pos % p.I[3], rest = pos / p.I[3];
+            const int row = rest % plane_rows, i0 = rest / plane_rows;
+            const int ph = i3 % S, m = i3 / S;
+            xp[((int64_t)((i0 * cg + g) * S + ph) * p.xp_rows + row) * mS + m] = x[e];
+        } else if (e < n_x + n_xz) {
+            const int f = e - n_x;
+            const int m = f % mS, r = f / mS;
+            const int row = plane_rows + r % tail, blk = r / tail;  // blk = (i0 * cg + g) * S + ph
+            xp[((int64_t)blk * p.xp_rows + row) * mS + m] = zero;
+        } else if (e < n_x + n_xz + n_w) {
+            const int f = e - n_x - n_xz;
+            const int g = f % cg, r = f / cg;
+            const int r3 = r % p.R[3], r2 = r / p.R[3];
+            const int trip = r2 % trips, o = r2 / trips;
+            const int j = p.R[3] + S - 2 - r3;
+            wp[((int64_t)(trip * cg + g) * p.nslices + j) * p.cout + o] = w[f];
+        } else {
+            const int f = e - n_x - n_xz - n_w;
+            const int o = f % p.cout, r = f / p.cout;
+            const int z = r % zs, r2 = r / zs;  // z < S - 1: the first slices, else the last
+            const int g = r2 % cg, trip = r2 / cg;
+            const int j = z < S - 1 ? z : p.R[3] + S - 1 + (z - (S - 1));
+            wp[((int64_t)(trip * cg + g) * p.nslices + j) * p.cout + o] = zero;
         }
     }
 }
@@ -411,11 +421,13 @@ int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t
     const int64_t last_row = (tiles - 1) * tile_pos / in[3] + (k[1] - 1) * in[2] + (k[2] - 1) + rows_box;
     if (last_row >= (1ll << 30)) return GEMM_ERR_UNSUPPORTED;
     p.xp_rows = (int)(last_row > in[1] * in[2] ? last_row : in[1] * in[2]);
-    // the staging kernel: 32-bit indices within a block, one grid row per block and triple
-    if ((int64_t)p.xp_rows * (in[3] / S) >= (1ll << 31) ||
-        in[0] * (cin / 8) * S + k[0] * k[1] * k[2] > 65535)
-        return GEMM_ERR_UNSUPPORTED;
     p.nslices = (int)(k[3] + 2 * S - 2);
+    // the staging kernel's flat index: every staged 16-byte chunk in 31 bits
+    const int64_t cgs = cin / 8, trips_all = k[0] * k[1] * k[2];
+    const int64_t chunks = in[0] * in[1] * in[2] * in[3] * cgs +
+                           in[0] * cgs * S * (p.xp_rows - in[1] * in[2]) * (in[3] / S) +
+                           cout * trips_all * k[3] * cgs + trips_all * cgs * (2 * S - 2) * cout;
+    if (chunks >= (1ll << 31) - (1ll << 20)) return GEMM_ERR_UNSUPPORTED;
     p.b_trip = (int)((cin / 8) * p.nslices * cout * 16);
     // MMA issuers: one per pair of TMEM accumulators' share, at most CT_MAX_ISSUERS
     const int N = S * p.cout;
@@ -508,14 +520,14 @@ int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void
     p.limit_ns = limit_ns;
     p.test_stall = test_stall;
 
-    // one grid row per staged-input block and per filter triple, enough blocks along x
-    // for about 4 waves in all
-    const int64_t nblk = (int64_t)p.I[0] * (cin / 8) * S;
-    const int64_t rows_y = nblk + (int64_t)p.R[0] * p.R[1] * p.R[2];
-    const int64_t per_y = std::max<int64_t>((int64_t)p.xp_rows * (p.I[3] / S), (cin / 8) * p.nslices * cout);
-    int64_t gx = (int64_t)num_sms * 4 * 8 / rows_y;  // 8 blocks of 256 threads per SM
-    gx = std::min<int64_t>(std::max<int64_t>(gx, 1), (per_y + 255) / 256);
-    conv_tc_prepare_kernel<<<dim3((unsigned)gx, (unsigned)rows_y), 256, 0, stream>>>(
+    // one 16-byte chunk per thread where one resident wave holds them all (8 blocks of 256
+    // threads per SM), a grid-stride loop beyond
+    const int64_t cgs = cin / 8, trips_all = (int64_t)p.R[0] * p.R[1] * p.R[2];
+    const int64_t chunks = (int64_t)p.I[0] * p.I[1] * p.I[2] * p.I[3] * cgs +
+                           (int64_t)p.I[0] * cgs * S * (p.xp_rows - p.I[1] * p.I[2]) * (p.I[3] / S) +
+                           (int64_t)cout * trips_all * p.R[3] * cgs + trips_all * cgs * (2 * S - 2) * cout;
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((chunks + 255) / 256, (int64_t)num_sms * 8));
+    conv_tc_prepare_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
         static_cast<const uint4*>(x), static_cast<const uint4*>(w), p, reinterpret_cast<uint4*>(ws),
         reinterpret_cast<uint4*>(ws + xb));
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
