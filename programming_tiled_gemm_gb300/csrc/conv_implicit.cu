@@ -78,6 +78,8 @@ __device__ __forceinline__ int64_t group_base(const ConvGeom& g, int q)
 template <bool VEC>
 __global__ void __launch_bounds__(CI_THREADS, 1) conv4d_implicit_kernel(ConvParams p)
 {
+    // the split-K reduction launched next may start its blocks now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int W_PER_THREAD = (CI_TAPS_PER_CHUNK * CI_MR + CI_THREADS - 1) / CI_THREADS;
     __shared__ __align__(16) float wsm[2][CI_TAPS_PER_CHUNK][CI_MR];  // weights, [tap][out channel]
     __shared__ int64_t gbase[2][CI_MAX_GROUPS_PER_CHUNK];

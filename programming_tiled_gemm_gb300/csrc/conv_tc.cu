@@ -538,17 +538,9 @@ int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void
         return GEMM_ERR_CUDA;
     // programmatic dependent launch: the CTAs set up their barriers and TMEM while the
     // staging kernel still runs; the producer waits for it before its first copy
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.tiles_per_p0 * p.P[0]));
-    cfg.blockDim = dim3(CT_THREADS);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, conv4d_tc_kernel, p) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (launch_dependent(conv4d_tc_kernel, dim3((unsigned)(p.tiles_per_p0 * p.P[0])), dim3(CT_THREADS), (size_t)smem,
+                         stream, p) != cudaSuccess)
+        return GEMM_ERR_CUDA;
     *launches += 1;
     return GEMM_OK;
 }

@@ -307,6 +307,9 @@ ffma_warptile_kernel(const float* __restrict__ A, int lda_, const float* __restr
                      float* __restrict__ C, int ldc_, int M, int N, int K, int k_per_split, TileMap tmap,
                      float* __restrict__ ws, int vec_in, int vec_out)
 {
+    // a programmatic dependent launched next (the last wave's K slices, or the reduction,
+    // which waits for this grid) may start as SMs free up
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t lda = lda_, ldb = ldb_, ldc = ldc_;
     extern __shared__ __align__(16) float w_smem[];
     float (*As)[W_BK][W_AS_LD] = reinterpret_cast<float (*)[W_BK][W_AS_LD]>(w_smem);
@@ -480,6 +483,7 @@ __global__ void __launch_bounds__(256)
 splitk_reduce_tiles_kernel(const float* __restrict__ ws, int split, TileMap tmap, int ntiles, float* __restrict__ C,
                            int64_t ldc)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the partials' writer has finished
     constexpr int TILE = W_BM * W_BN;
     const int64_t total = (int64_t)ntiles * TILE / 4;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -504,6 +508,7 @@ __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float* __restrict__ ws, int split, int64_t M, int64_t N,
                      float* __restrict__ C, int64_t ldc)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the partials' writer has finished
     const int64_t total = M * N;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
@@ -625,14 +630,16 @@ cudaError_t launch_warptile(const F32Args& a, int split, float* ws, int remainde
             TileMap tr = t;
             tr.first = main_tiles;
             tr.compact = 1;
-            ffma_warptile_kernel<false><<<dim3(rem, 1, rsplit), kThreads, W_SMEM_BYTES, stream>>>(
-                a.A, (int)a.lda, a.B, (int)a.ldb, a.C, (int)a.ldc, (int)a.M, (int)a.N, (int)a.K, (int)rkps, tr, ws, vec_in, vec_out);
-            cudaError_t e = cudaGetLastError();
+            // the K slices read nothing the full waves write (their partials go to the
+            // workspace), so they start on SMs as the last full wave drains
+            cudaError_t e = launch_dependent(ffma_warptile_kernel<false>, dim3(rem, 1, rsplit), dim3(kThreads),
+                                             W_SMEM_BYTES, stream, a.A, (int)a.lda, a.B, (int)a.ldb, a.C, (int)a.ldc,
+                                             (int)a.M, (int)a.N, (int)a.K, (int)rkps, tr, ws, vec_in, vec_out);
             if (e != cudaSuccess) return e;
             int64_t blocks = (int64_t)rem * W_BM * W_BN / 4 / 256;
             if (blocks < 1) blocks = 1;
-            splitk_reduce_tiles_kernel<<<(unsigned)blocks, 256, 0, stream>>>(ws, rsplit, tr, rem, a.C, a.ldc);
-            e = cudaGetLastError();
+            e = launch_dependent(splitk_reduce_tiles_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, ws, rsplit,
+                                 tr, rem, a.C, a.ldc);
             if (e != cudaSuccess) return e;
             *launches += 2;
         }
@@ -709,8 +716,8 @@ cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t 
     const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 152) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(ws, split, M, N, C, ldc);
-    return cudaGetLastError();
+    return launch_dependent(splitk_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, ws, split, M, N, C,
+                            ldc);
 }
 
 }  // namespace gemm_gb300

@@ -57,7 +57,30 @@ int skinny_tma_auto_split(const F32Args& a, int num_sms);
 cudaError_t launch_skinny_tma(const F32Args& a, int split, float* workspace, int num_sms, int* dev_status,
                               uint64_t limit_ns, int test_stall, cudaStream_t stream, int* launches);
 
-// Fixed-order split-K reduction: C[m][n] = sum_{s=0..split-1} ws[s][m][n].
+// Launch `kern` as a programmatic dependent of the kernel before it on `stream`: its
+// blocks may start once every block of that kernel has run griddepcontrol.launch_dependents
+// (or it has finished); a kernel that reads what that one writes runs griddepcontrol.wait
+// first.  Work queued after it still waits for both.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Fixed-order split-K reduction: C[m][n] = sum_{s=0..split-1} ws[s][m][n]; launched as a
+// programmatic dependent of the kernel that wrote `ws` (it waits for that kernel before
+// reading).
 cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t N, float* C,
                                  int64_t ldc, int num_sms, cudaStream_t stream);
 

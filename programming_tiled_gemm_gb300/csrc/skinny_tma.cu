@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(StCfg<MR, COLW, MSPLIT, KROWS, CPT>::THREADS, 
 skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
 {
     using SM = StCfg<MR, COLW, MSPLIT, KROWS, CPT>;
+    // the split-K reduction launched next may start its blocks now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int NQ = CPT / 4;  // column quads per thread
     constexpr int ST_KROWS = KROWS;
     constexpr int ST_STAGES = SM::STAGES;
