@@ -187,6 +187,25 @@ def test_last_wave_tiles_split_along_K(lib, M, N):
     assert np.abs(got - ref_of(A, B)).max() <= 1e-5 * math.sqrt(K)
 
 
+def test_back_to_back_split_products_share_the_workspace(lib):
+    """Products whose K slices or split-K partials go through the handle's workspace,
+    queued on one stream with no synchronisation in between: the later launches of one
+    call start as the earlier ones drain (programmatic dependent launches), and the next
+    call's partials must not overwrite a workspace that is still being read."""
+    shapes = [(1664, 3328, 2048), (16, 4096, 8192), (1664, 3328, 1024), (32, 1000, 3000)]
+    ops = []
+    for i, (M, N, K) in enumerate(shapes):
+        Ai, Bi = si.integer_copy(M, N, K, seed=100 + i)
+        ops.append((Ai, Bi, Ai.cuda(), Bi.cuda(), torch.empty((M, N), device="cuda")))
+    torch.cuda.synchronize()
+    for _, _, Ad, Bd, C in ops:
+        lib.matmul(Ad, Bd, out=C)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    for Ai, Bi, _, _, C in ops:
+        assert np.array_equal(C.cpu().double().numpy(), ref_of(Ai, Bi))
+
+
 def test_results_are_deterministic(lib):
     import programming_tiled_gemm_gb300 as g
     A, B = si.gemm_operands(24, 3000, 5000, seed=9)
