@@ -372,8 +372,8 @@ std::vector<int64_t> host_chunk_rows(const gemm_host_problem& q)
     if (q.M <= 0 || q.N <= 0) return rows;
     auto up256 = [](int64_t v) { return (v + 255) / 256 * 256; };
     if (q.K > 0 && q.dtype == GEMM_F32 && q.M >= 4096) {
-        const int64_t a = up256(q.M / 2), b = up256(q.M * 3 / 8);
-        rows = {a, b, q.M - a - b};
+        const int64_t a = up256(q.M / 8), b = up256(q.M * 3 / 8);
+        rows = {a, b, b, q.M - a - 2 * b};
     } else if (q.K > 0 && q.dtype != GEMM_F32 && q.M >= 2048) {
         int64_t n = q.M / 4096;
         n = n < 2 ? 2 : (n > 4 ? 4 : n);
