@@ -372,8 +372,15 @@ std::vector<int64_t> host_chunk_rows(const gemm_host_problem& q)
     if (q.M <= 0 || q.N <= 0) return rows;
     auto up256 = [](int64_t v) { return (v + 255) / 256 * 256; };
     if (q.K > 0 && q.dtype == GEMM_F32 && q.M >= 4096) {
+        // 1/8, 3/8, 3/8 and the rest, each rounded up to 256 rows and cut to what is left
         const int64_t a = up256(q.M / 8), b = up256(q.M * 3 / 8);
-        rows = {a, b, b, q.M - a - 2 * b};
+        int64_t left = q.M;
+        for (int64_t want : {a, b, b}) {
+            const int64_t r = want < left ? want : left;
+            if (r > 0) rows.push_back(r);
+            left -= r;
+        }
+        if (left > 0) rows.push_back(left);
     } else if (q.K > 0 && q.dtype != GEMM_F32 && q.M >= 2048) {
         int64_t n = q.M / 4096;
         n = n < 2 ? 2 : (n > 4 ? 4 : n);

@@ -310,7 +310,8 @@ def test_host_batch_pipelines_several_products(lib):
     padded host leading dimensions and an empty one, in one pipeline; integer inputs: exact,
     and each result equals the single-product entry point's."""
     import programming_tiled_gemm_gb300 as g
-    shapes = [(4352 + 3, 264, 72, "bf16"), (4100, 136, 40, "f32"), (300, 72, 520, "f16"), (0, 8, 8, "bf16")]
+    shapes = [(4352 + 3, 264, 72, "bf16"), (4100, 136, 40, "f32"), (300, 72, 520, "f16"), (0, 8, 8, "bf16"),
+              (4863, 16, 8, "f32"), (4864, 24, 16, "f32")]  # fp32 row chunks rounded past M, or ending at M
     pairs, outs, refs = [], [], []
     for i, (M, N, K, dt) in enumerate(shapes):
         A, B = si.integer_copy(M, N, K, seed=60 + i, dtype=dt)
