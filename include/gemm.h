@@ -74,7 +74,9 @@ int gemm_destroy(gemm_handle_t h);
 /* C = A . B (alpha = 1, beta = 0; C is overwritten, never read).
  *   M, N, K  >= 0.  M == 0 or N == 0: nothing is done.  K == 0: C is set to zero.
  *   lda >= K, ldb >= N, ldc >= N (elements).  Rows may be padded; padding is never
- *   read or written.
+ *   read or written.  Every size and leading dimension must stay below 2^31 - 1024
+ *   (the kernels index in 32 bits), else GEMM_ERR_UNSUPPORTED before anything is
+ *   allocated or launched.
  *   dtype GEMM_F32: A, B are float*; any alignment (16-byte aligned bases and ld % 4
  *   == 0 take the vectorised loads).
  *   dtype GEMM_BF16 / GEMM_F16: A, B are 16-bit; A, B must be 16-byte aligned and

@@ -78,6 +78,7 @@ int ensure_buffer(void** buf, size_t* have, size_t bytes)
     size_t want = bytes < 256 ? 256 : bytes;
     if (cudaMalloc(buf, want) != cudaSuccess) {
         *buf = nullptr;
+        (void)cudaGetLastError();  // an allocation failure is not sticky: keep it out of later launch checks
         return GEMM_ERR_CUDA;
     }
     *have = want;
@@ -102,6 +103,14 @@ int check_common(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A
     if (M > lim / (ldc > 0 ? ldc : 1) || (K > 0 && (M > lim / lda || K > lim / ldb)))
         return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
+}
+
+// Every kernel indexes with 32-bit sizes and leading dimensions: larger ones are refused
+// before anything is allocated or launched.
+bool beyond_kernel_limits(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc)
+{
+    constexpr int64_t kLim32 = 0x7fffffffLL - 1024;
+    return M > kLim32 || N > kLim32 || K > kLim32 || ldc > kLim32 || (K > 0 && (lda > kLim32 || ldb > kLim32));
 }
 
 int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)
@@ -238,6 +247,7 @@ int gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha, c
     if (rc != GEMM_OK) return rc;
     if (c_dtype != GEMM_F32 && c_dtype != GEMM_BF16 && c_dtype != GEMM_F16) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
+    if (beyond_kernel_limits(M, N, K, lda, ldb, ldc)) return GEMM_ERR_UNSUPPORTED;
     const size_t ces = (c_dtype == GEMM_F32) ? 4 : 2;
     if (reinterpret_cast<uintptr_t>(C) & (ces - 1)) return GEMM_ERR_ALIGNMENT;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -449,6 +459,8 @@ int run_host_problems(gemm_handle_t h, int count, const gemm_host_problem* q, vo
         const int rc = check_common(h, q[i].M, q[i].N, q[i].K, q[i].A, q[i].lda, q[i].B, q[i].ldb, q[i].C, q[i].ldc,
                                     q[i].dtype);
         if (rc != GEMM_OK) return rc;
+        if (q[i].M > 0 && q[i].N > 0 && beyond_kernel_limits(q[i].M, q[i].N, q[i].K, q[i].lda, q[i].ldb, q[i].ldc))
+            return GEMM_ERR_UNSUPPORTED;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     DeviceGuard g(h->device);

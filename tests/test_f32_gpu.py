@@ -238,6 +238,36 @@ def test_argument_errors_are_reported(lib):
     assert g.gemm_run(h, 4, 3, 4, A.data_ptr(), 4, A.data_ptr(), 3, C.data_ptr(), 4, 0) == g.GEMM_ERR_ALIGNMENT
 
 
+def test_sizes_beyond_the_kernels_and_failed_allocations_leave_the_handle_usable(lib):
+    """A size or leading dimension past the kernels' 32-bit indexing is refused before
+    anything is allocated or launched; a workspace too large to allocate is reported as a
+    CUDA error; neither leaves an error behind for the next call."""
+    import programming_tiled_gemm_gb300 as g
+    h = lib.handle
+    A = torch.ones(64, device="cuda")
+    C = torch.zeros(64, device="cuda")
+    big = 2**31 - 1
+    assert g.gemm_run(h, big, 4, 4, A.data_ptr(), 4, A.data_ptr(), 4, C.data_ptr(), 4, 0) == g.GEMM_ERR_UNSUPPORTED
+    assert g.gemm_run(h, 4, 4, 4, A.data_ptr(), big, A.data_ptr(), 4, C.data_ptr(), 4, 0) == g.GEMM_ERR_UNSUPPORTED
+    assert g.gemm_run(h, 4, 4, 4, A.data_ptr(), 8, A.data_ptr(), 8, C.data_ptr(), 4, g.GEMM_BF16) == g.GEMM_OK
+    torch.cuda.synchronize()
+    assert g.gemm_run(h, 4, big, 4, A.data_ptr(), 8, A.data_ptr(), big, C.data_ptr(), big,
+                      g.GEMM_BF16) == g.GEMM_ERR_UNSUPPORTED
+    # 1024 K slices of a 65536 x 65536 product: a ~17.6 TB workspace that cudaMalloc refuses
+    lib.set_option(g.GEMM_OPT_SPLIT_K, 1024)
+    try:
+        n = 65536
+        assert g.gemm_run(h, n, n, 1024, A.data_ptr(), 1024, A.data_ptr(), n, C.data_ptr(), n, 0) == g.GEMM_ERR_CUDA
+    finally:
+        lib.set_option(g.GEMM_OPT_SPLIT_K, 0)
+    # the handle and the thread's CUDA state are clean: a normal product runs and is exact
+    Ai, Bi = si.integer_copy(40, 72, 56, seed=77)
+    got = lib.matmul(Ai.cuda(), Bi.cuda())
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    assert np.array_equal(got.cpu().double().numpy(), ref_of(Ai, Bi))
+
+
 def test_host_buffer_entry_point(lib):
     A, B = si.integer_copy(70, 90, 110, seed=4)
     C = lib.matmul_host(A, B)
