@@ -216,8 +216,8 @@ typedef enum {
                                    128x256 tiles that fill under half the SMs, K split into 2 to 16 slices,
                                    one CTA each, on a cluster per tile that adds the fp32 partial tiles in
                                    slice order through distributed shared memory), 1 one CTA per
-                                   128x256 tile, 2 a pair of CTAs (cluster of two) per 256x256 tile, 3 two
-                                   pairs (cluster of four) per 512x256 tile, B read once for both pairs */
+                                   128x256 tile, 2 a pair of CTAs (cluster of two) per 256x256 tile.  Any
+                                   other value (3 included) is GEMM_ERR_INVALID_ARG */
     GEMM_OPT_TEST_STALL = 6,    /* test hook for failure detection, 0 (default) or 1: the kernels with
                                    bounded waits (tensor-core GEMMs and convolution, TMA skinny GEMM) first wait on a
                                    barrier nothing arrives on; the wait runs out after the wait limit, the

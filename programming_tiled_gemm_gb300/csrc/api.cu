@@ -32,7 +32,7 @@ struct gemm_ctx {
     int opt_f32_kernel = 0;
     int opt_split_k = 0;
     int opt_tc_chunk = 0;  // tensor-core accumulation chunk in 64-wide k-blocks (0 = default)
-    int opt_tc_pair = 0;   // tensor-core tile: 0 choose, 1 single CTA, 2 CTA pair, 3 two pairs
+    int opt_tc_pair = 0;   // tensor-core tile: 0 choose, 1 single CTA, 2 CTA pair
     int opt_test_stall = 0;  // test hook: kernels with bounded waits let one wait run out
     int opt_conv_stack = 0;  // tensor-core convolution: output positions stacked along N (0 = choose)
     uint64_t wait_limit_ns = 2000000000ull;
@@ -219,7 +219,7 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
         h->opt_tc_chunk = (int)value;
         return GEMM_OK;
     case GEMM_OPT_TC_PAIR:
-        if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
         h->opt_tc_pair = (int)value;
         return GEMM_OK;
     case GEMM_OPT_CONV_STACK:

@@ -143,8 +143,7 @@ struct TcWorkspace {
 TcWorkspace tc_workspace_need(const TcArgs& a, int num_sms, int pair_mode);
 // Returns GEMM_OK or a negative gemm_status_t.
 // kc_blocks: 64-wide k-blocks per accumulation chunk (0 = default 16).
-// pair_mode: 0 = choose, 1 = single-CTA 128 x 256 tiles, 2 = CTA-pair 256 x 256 tiles,
-// 3 = two CTA pairs sharing B.
+// pair_mode: 0 = choose, 1 = single-CTA 128 x 256 tiles, 2 = CTA-pair 256 x 256 tiles.
 // With pair_mode 0, M <= 128 and tiles that fill under half the SMs, K is split into
 // slices run by the CTAs of one cluster per tile (no workspace).
 int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_limit_ns, int kc_blocks,

@@ -722,19 +722,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// The same load multicast to the CTAs of `mask` (cluster ranks): the box lands at this
-// shared-memory offset in each of them, and each delivery is counted on the barrier at
-// `bar_cluster`'s offset in the even CTA of the receiving CTA's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
-                                                    int x, int y, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "h"(mask)
-        : "memory");
-}
-
 // Arrive on the barrier at this offset in every CTA of `mask` once every tcgen05.mma
 // issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit_mask(uint32_t bar, uint16_t mask)
@@ -754,13 +741,9 @@ __device__ __forceinline__ void grace_period(uint64_t ns)
     }
 }
 
-// PAIRS = 1: a cluster is one CTA pair computing 256 x 256 tiles.
-// PAIRS = 2: a cluster of four CTAs is two pairs computing the two 256-row halves of a
-// 512 x 256 tile.  Both pairs need the same columns of B, so each B half is read from L2
-// once for both: the CTA of each pair loads 32 of the 64 k-rows of its half and
-// multicasts them to the CTA holding the same half in the other pair.  A stage is then
-// free only when both pairs' MMAs are done with it (two arrivals on "empty").
-template <int P_STAGES, int PAIRS>
+// A cluster is one CTA pair computing 256 x 256 tiles; each CTA loads its own operand
+// halves with plain (per-CTA) TMA loads.
+template <int P_STAGES>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, TcParams p)
@@ -783,19 +766,16 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const uint32_t crank = cluster_ctarank();
-    const uint32_t rank = crank & 1;         // CTA within its pair
-    const int pq = (int)(crank >> 1);        // pair within the cluster
-    const uint32_t leader = crank & ~1u;     // the pair's even CTA (issues its MMAs)
-    const uint16_t pair_mask = (uint16_t)(0x3u << (2 * pq));
-    const uint16_t all_mask = (uint16_t)((1u << (2 * PAIRS)) - 1);
-    const int pair = blockIdx.x / (2 * PAIRS);   // cluster index: walks cluster tiles
-    const int npairs = gridDim.x / (2 * PAIRS);
+    const uint32_t rank = cluster_ctarank();  // CTA within its pair
+    const uint32_t leader = 0;                 // the pair's even CTA (issues its MMAs)
+    const uint16_t pair_mask = 0x3;
+    const int pair = blockIdx.x / 2;  // cluster index: walks pair tiles
+    const int npairs = gridDim.x / 2;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < P_STAGES; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), PAIRS);  // one commit per pair reading the stage
+            mbar_init(smem_u32(&empty_bar[s]), 1);  // the pair's commit
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
@@ -838,22 +818,12 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t fb_even = mapa_shared(fb_local, leader);
                     if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
                     tma_load_2d_pair(smem_u32(smem_a + stage * P_A_STAGE_BYTES), &tmA, fb_even, kb * BK,
-                                     (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM);
+                                     tc.m_blk * (2 * BM) + (int)rank * BM);
                     uint8_t* b_dst = smem_b + stage * P_B_STAGE_BYTES;
-                    if (PAIRS == 1) {
 #pragma unroll
-                        for (int j = 0; j < (BN / 2) / B_BOX_N; ++j)
-                            tma_load_2d_pair(smem_u32(b_dst + j * B_BOX_BYTES), &tmB, fb_even,
-                                             tc.n_blk * BN + (int)rank * (BN / 2) + j * B_BOX_N, kb * BK);
-                    } else {
-                        // k-rows [32 pq, 32 pq + 32) of this CTA's B half, to both pairs
-                        const uint16_t mc = (uint16_t)((1u << rank) | (1u << (rank + 2)));
-#pragma unroll
-                        for (int j = 0; j < (BN / 2) / B_BOX_N; ++j)
-                            tma_load_2d_pair_mc(smem_u32(b_dst + j * B_BOX_BYTES + pq * (BK / 2) * 128), &tmB,
-                                                fb_even, tc.n_blk * BN + (int)rank * (BN / 2) + j * B_BOX_N,
-                                                kb * BK + pq * (BK / 2), mc);
-                    }
+                    for (int j = 0; j < (BN / 2) / B_BOX_N; ++j)
+                        tma_load_2d_pair(smem_u32(b_dst + j * B_BOX_BYTES), &tmB, fb_even,
+                                         tc.n_blk * BN + (int)rank * (BN / 2) + j * B_BOX_N, kb * BK);
                     if (++stage == P_STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -901,7 +871,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             const uint64_t b_desc = smem_desc_sw128(b_st + k * UMMA_K * 128, B_BOX_BYTES, 1024);
                             umma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         }
-                        umma_commit_mask(smem_u32(&empty_bar[stage]), all_mask);  // every CTA that filled it
+                        umma_commit_mask(smem_u32(&empty_bar[stage]), pair_mask);  // both CTAs that filled it
                         if (++stage == P_STAGES) {
                             stage = 0;
                             phase ^= 1;
@@ -996,7 +966,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 n = __shfl_sync(0xffffffffu, n, 0);
                 uint8_t* stg = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
-                const int row0 = (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM + q * 32;
+                const int row0 = tc.m_blk * (2 * BM) + (int)rank * BM + q * 32;
                 const int col0 = tc.n_blk * BN + half * EPI_COLS;
                 if (n == 1) {
                     store_rows_tma<false>(&tmC, tot, stg, row0, col0, p.M, p.N, lane);
@@ -1032,9 +1002,9 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (w.sl >= 0 && !rem_slice_combine(p, tot, t - p.rem_first, w.sl, (int)rank, warp - 2, lane, p.status,
                                                 abort_flag))
                 continue;
-            const int row = (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM + q * 32 + lane;
+            const int row = tc.m_blk * (2 * BM) + (int)rank * BM + q * 32 + lane;
             if (p.c_tma) {
-                store_rows_tma(&tmC, tot, epi_stage + (warp - 2) * EPI_STAGE_BYTES, (tc.m_blk * PAIRS + pq) * (2 * BM) + (int)rank * BM + q * 32,
+                store_rows_tma(&tmC, tot, epi_stage + (warp - 2) * EPI_STAGE_BYTES, tc.m_blk * (2 * BM) + (int)rank * BM + q * 32,
                                tc.n_blk * BN + half * EPI_COLS, p.M, p.N, lane);
             } else if (row < p.M && !p.epi_plain) {
                 const int col0 = tc.n_blk * BN + half * EPI_COLS;
@@ -1178,25 +1148,24 @@ int choose_split(int64_t tiles, int64_t k_blocks, int num_sms)
 
 namespace {
 
-// Clusters of the CTA-pair kernel (PAIRS pairs each) resident at once (0: unknown).
+// Clusters of the CTA-pair kernel resident at once (0: unknown).
 // Cached per process: every device a process drives is taken to be the same part.
-template <int PAIRS>
 int pair_clusters_fit()
 {
     static std::atomic<int> cache{-1};
     int v = cache.load();
     if (v >= 0) return v;
     v = 0;
-    auto kern = tc_gemm_pair_kernel<P_STAGES_DEFAULT, PAIRS>;
+    auto kern = tc_gemm_pair_kernel<P_STAGES_DEFAULT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem_bytes(P_STAGES_DEFAULT)) ==
         cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * PAIRS, 1, 1);
+        cfg.gridDim = dim3(2, 1, 1);
         cfg.blockDim = dim3(THREADS, 1, 1);
         cfg.dynamicSmemBytes = p_smem_bytes(P_STAGES_DEFAULT);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2 * PAIRS;
+        attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
@@ -1210,7 +1179,7 @@ int pair_clusters_fit()
 
 // How a product is laid on the tensor-core kernels.
 struct TcPlan {
-    bool pair = false, quad = false;
+    bool pair = false;
     int64_t tiles = 0;    // output tiles of the chosen kernel
     int clusters = 0;     // pair kernels: clusters launched
     int rem_first = 0;    // pair kernel: first split tile (tiles = none)
@@ -1224,8 +1193,7 @@ TcPlan plan_tc(const TcArgs& a, int num_sms, int pair_mode)
 {
     TcPlan pl;
     pl.c_tma = a.epi.plain() && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0;
-    pl.quad = (pair_mode == 3) && num_sms >= 4;
-    pl.pair = pl.quad || (pair_mode == 2) || (pair_mode == 0 && a.M > BM && num_sms >= 2);
+    pl.pair = (pair_mode == 2) || (pair_mode == 0 && a.M > BM && num_sms >= 2);
     const int64_t n_blocks = (a.N + BN - 1) / BN;
     const int64_t k_blocks = (a.K + BK - 1) / BK;
     const int64_t single_tiles = ((a.M + BM - 1) / BM) * n_blocks;
@@ -1235,12 +1203,11 @@ TcPlan plan_tc(const TcArgs& a, int num_sms, int pair_mode)
         if (pair_mode == 0 && !a.test_stall && a.M <= BM) pl.single_split = choose_split(single_tiles, k_blocks, num_sms);
         return pl;
     }
-    const int cl = pl.quad ? 4 : 2;
-    pl.tiles = ((a.M + cl * BM - 1) / (cl * BM)) * n_blocks;
+    pl.tiles = ((a.M + 2 * BM - 1) / (2 * BM)) * n_blocks;
     // a persistent grid must be co-resident: clusters are placed within one GPC each, so
-    // fewer than num_sms / cl of them may fit
-    int64_t clusters = num_sms / cl;
-    const int fit = pl.quad ? pair_clusters_fit<2>() : pair_clusters_fit<1>();
+    // fewer than num_sms / 2 of them may fit
+    int64_t clusters = num_sms / 2;
+    const int fit = pair_clusters_fit();
     if (fit > 0 && fit < clusters) clusters = fit;
     pl.rem_first = (int)pl.tiles;
     // the tiles of a last wave that leaves pairs idle are cut along K (CTA pairs only;
@@ -1248,7 +1215,7 @@ TcPlan plan_tc(const TcArgs& a, int num_sms, int pair_mode)
     // published to L2, counted, the others read back), so every slice keeps at least 32
     // k-blocks (about 11 us of MMAs on a pair): shorter slices measured slower than none.
     const int64_t r = pl.tiles % clusters;  // tiles of the last wave (all of them if fewer than pairs)
-    if (!pl.quad && !a.test_stall && r != 0) {
+    if (!a.test_stall && r != 0) {
         int64_t sp = clusters / r;
         if (sp > MAX_REM_SPLIT) sp = MAX_REM_SPLIT;
         while (sp > 1 && k_blocks / sp < 32) --sp;
@@ -1324,10 +1291,8 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.status = dev_status;
     p.limit_ns = wait_limit_ns;
     p.test_stall = a.test_stall;
-    // CTA pairs: 256 x 256 tiles on clusters of two (or 512 x 256 tiles on clusters of
-    // two pairs sharing B); single CTAs: 128 x 256 tiles
+    // CTA pairs: 256 x 256 tiles on clusters of two; single CTAs: 128 x 256 tiles
     const TcPlan pl = plan_tc(a, num_sms, pair_mode);
-    const bool use_quad = pl.quad;
     p.num_items = p.num_tiles;
     p.rem_first = p.num_tiles;
     p.rem_split = 1;
@@ -1337,8 +1302,7 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
     p.rem_seq = 0;
     p.rem_direct = 0;
     if (pl.pair) {
-        const int pairs_per_cluster = use_quad ? 2 : 1;
-        const int cl = 2 * pairs_per_cluster;  // CTAs per cluster
+        const int cl = 2;  // CTAs per cluster
         p.m_blocks = (int)((a.M + cl * BM - 1) / (cl * BM));
         const int64_t ctiles = (int64_t)p.m_blocks * p.n_blocks;
         p.num_tiles = (int)ctiles;
@@ -1360,11 +1324,8 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
         // 6 stages of 32 KiB; 7 measured no faster.  Raster groups of 2048 rows of C
         // (8 pair tiles) measured best among 512 .. 4096 rows, within run-to-run noise.
         constexpr int stages = P_STAGES_DEFAULT;
-        p.group_m = 8 / pairs_per_cluster;
-        CUtensorMap tmBq = tmB;
-        if (use_quad && !encode_2d(&tmBq, a.B, bf16, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.ldb, B_BOX_N, BK / 2))
-            return GEMM_ERR_CUDA;
-        auto kern = use_quad ? tc_gemm_pair_kernel<stages, 2> : tc_gemm_pair_kernel<stages, 1>;
+        p.group_m = 8;
+        auto kern = tc_gemm_pair_kernel<stages>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem_bytes(stages)) !=
             cudaSuccess)
             return GEMM_ERR_CUDA;
@@ -1380,7 +1341,7 @@ int launch_tc_gemm(const TcArgs& a, int num_sms, int* dev_status, uint64_t wait_
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, kern, tmA, use_quad ? tmBq : tmB, tmC, p) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p) != cudaSuccess) return GEMM_ERR_CUDA;
         *launches += 1;
         return GEMM_OK;
     }

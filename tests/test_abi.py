@@ -81,3 +81,15 @@ def test_create_without_a_gpu_reports_an_error(pkg):
     rc = pkg.library().gemm_create(ctypes.byref(h), 0)
     assert rc in (pkg.GEMM_ERR_CUDA, pkg.GEMM_ERR_INVALID_ARG)
     assert not h.value
+
+
+def test_no_multicast_bulk_copy_in_the_sources():
+    """The library may run as one replica per GPU of a node, so no bulk (TMA) copy in its
+    sources multicasts to the CTAs of a cluster; the CTA-pair kernel loads its operand
+    halves per CTA.  (The pair's MMA commit, which signals barriers in both CTAs of the
+    pair, is not a copy.)"""
+    csrc = os.path.join(ROOT, "programming_tiled_gemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, name)).read()
+        for stmt in re.findall(r"cp\.(?:async|reduce\.async)\.bulk[^;\"]*", text):
+            assert "multicast" not in stmt, (name, stmt)

@@ -22,7 +22,6 @@ GUARD = 2
 
 PATHS = [  # (name, input dtype, M, N, K, tc pair option)
     ("tc_pair", "bf16", 520, 264, 136, 2),
-    ("tc_two_pairs", "bf16", 600, 264, 136, 3),
     ("tc_single", "f16", 300, 264, 72, 1),
     ("tc_split_k", "bf16", 100, 1000, 1100, 0),  # M <= 128, 4 tiles: K in 2 slices
     ("tc_pair_last_wave", "bf16", 520, 264, 4160, 2),  # 6 pair tiles, each in 2 K slices

@@ -70,12 +70,11 @@ SHAPES = [(1, 1, 1), (128, 256, 64), (128, 256, 16), (129, 257, 65), (200, 300, 
           (256, 512, 1024), (1000, 24, 520), (1024, 2048, 512), (2048, 4096, 384)]
 
 
-@pytest.mark.parametrize("pair", [1, 2, 3])
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_integer_inputs_exact(lib, pair, dtype, M, N, K):
-    """pair 1: one CTA per 128 x 256 tile; pair 2: CTA pairs (cta_group::2) per 256 x 256 tile;
-    pair 3: two pairs (cluster of four, B multicast) per 512 x 256 tile."""
+    """pair 1: one CTA per 128 x 256 tile; pair 2: CTA pairs (cta_group::2) per 256 x 256 tile."""
     import programming_tiled_gemm_gb300 as g
     lib.set_option(g.GEMM_OPT_TC_PAIR, pair)
     A, B = si.integer_copy(M, N, K, seed=M + 3 * N + 7 * K, dtype=dtype)
@@ -83,7 +82,7 @@ def test_integer_inputs_exact(lib, pair, dtype, M, N, K):
     assert np.array_equal(got, oracle.gemm(A.float().numpy(), B.float().numpy()))
 
 
-@pytest.mark.parametrize("pair", [1, 2, 3])
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("chunk", [1, 3, 16, 4096])
 def test_accumulation_chunks_exact(lib, pair, chunk):
     import programming_tiled_gemm_gb300 as g
@@ -94,7 +93,7 @@ def test_accumulation_chunks_exact(lib, pair, chunk):
     assert np.array_equal(got, oracle.gemm(A.float().numpy(), B.float().numpy()))
 
 
-@pytest.mark.parametrize("pair", [1, 2, 3])
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (384, 256, 4096), (200, 300, 8192)])
 def test_normal_bf16_within_tolerance(lib, pair, M, N, K):
     import programming_tiled_gemm_gb300 as g
@@ -103,6 +102,15 @@ def test_normal_bf16_within_tolerance(lib, pair, M, N, K):
     got = run_guarded(lib, A, B)
     err = np.abs(got - oracle.gemm(A.float().numpy(), B.float().numpy())).max()
     assert err <= 2e-5 * math.sqrt(K), err
+
+
+def test_tile_option_accepts_single_and_pair_only(lib):
+    """GEMM_OPT_TC_PAIR takes 0 (choose), 1 (single CTA) or 2 (CTA pair); nothing else."""
+    import programming_tiled_gemm_gb300 as g
+    for bad in (3, 4, -1):
+        with pytest.raises(g.GemmError) as e:
+            lib.set_option(g.GEMM_OPT_TC_PAIR, bad)
+        assert e.value.status == g.GEMM_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("M,N,K", [(1024, 2048, 2048), (4096, 4096, 4096)])
@@ -114,7 +122,7 @@ def test_results_are_deterministic(lib, M, N, K):
     A, B = si.gemm_operands(M, N, K, seed=5, dist="normal", dtype="bf16")
     Ad, Bd = A.cuda(), B.cuda()
     ref = None
-    for pair in (0, 1, 2, 3):
+    for pair in (0, 1, 2):
         lib.set_option(g.GEMM_OPT_TC_PAIR, pair)
         c1 = lib.matmul(Ad, Bd).clone()
         for _ in range(2):
