@@ -64,14 +64,29 @@ typedef enum {
 
 /* Create a handle bound to CUDA device `device`.  Queries the SM count, allocates the
  * device status word.  The caller's current device is restored before returning.
- * Fails with GEMM_ERR_UNSUPPORTED unless the device is compute capability 10.3. */
+ * Fails with GEMM_ERR_UNSUPPORTED unless the device is compute capability 10.3.
+ * The handle is the set-up step of the host program in "Learning to develop for GPU with
+ * GEMM as the example", section "Writing a GPU implementation of matrix multiplication"
+ * (its part on initialising the device: a device chosen by index and a context built on
+ * it; the command queue there is the caller's CUDA stream here), and it owns the extra
+ * memory that "Three X: large convolutions in PyTorch for training", section "How to call
+ * a convolution in the CUTLASS library", has the caller query and provide before the
+ * operation is initialised (here it is sized and grown by the library). */
 int gemm_create(gemm_handle_t* out, int device);
 
 /* Destroy a handle and free the memory it owns (not caller memory).  The handle's
- * streams must be idle (the call synchronises the device).  NULL is a no-op. */
+ * streams must be idle (the call synchronises the device).  NULL is a no-op.
+ * The end of the life cycle whose start is gemm_create: the device objects of "Learning
+ * to develop for GPU with GEMM as the example", section "Writing a GPU implementation of
+ * matrix multiplication", and the workspace of "Three X: large convolutions in PyTorch for
+ * training", section "How to call a convolution in the CUTLASS library". */
 int gemm_destroy(gemm_handle_t h);
 
-/* C = A . B (alpha = 1, beta = 0; C is overwritten, never read).
+/* C = A . B (alpha = 1, beta = 0; C is overwritten, never read): the product of
+ * "Learning to develop for GPU with GEMM as the example", section "Matrix product", with
+ * the argument list (m, n, k, a, b, c) that section "Writing a GPU implementation of
+ * matrix multiplication" hands its kernel, plus leading dimensions, the type and a
+ * stream in place of the command queue.
  *   M, N, K  >= 0.  M == 0 or N == 0: nothing is done.  K == 0: C is set to zero.
  *   lda >= K, ldb >= N, ldc >= N (elements).  Rows may be padded; padding is never
  *   read or written.  Every size and leading dimension must stay below 2^31 - 1024
@@ -107,7 +122,10 @@ int gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha,
                 const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
                 void* C, int64_t ldc, gemm_dtype_t ab_dtype, gemm_dtype_t c_dtype, void* stream);
 
-/* The same product with A, B and C in HOST memory (pageable or pinned).  A and B are
+/* The same product with A, B and C in HOST memory (pageable or pinned): the whole host
+ * program of "Learning to develop for GPU with GEMM as the example", section "Writing a
+ * GPU implementation of matrix multiplication" (copy the inputs to device buffers,
+ * enqueue the kernel, read the result back), with the copies overlapped with compute.  A and B are
  * copied into handle-owned device buffers and C is copied back, on two internal
  * streams ordered after the work already queued on `stream`; the product runs on
  * `stream`.  Large products are pipelined over row chunks (a multiple of 256 rows;
@@ -132,7 +150,9 @@ typedef struct gemm_host_problem {
     int dtype; /* gemm_dtype_t of A and B */
 } gemm_host_problem;
 
-/* Several host-memory products as one pipeline: each is staged in its own region of the
+/* Several host-memory products as one pipeline (the host program of "Learning to develop
+ * for GPU with GEMM as the example", section "Writing a GPU implementation of matrix
+ * multiplication", run for a list of products): each is staged in its own region of the
  * handle's device buffer and split into row chunks as in gemm_run_host.  The chunks run
  * on `stream` with half of the compute-bound products' chunks first, the transfer-bound
  * products' chunks next and the rest last (chunks of one product in order), so copies in
@@ -195,14 +215,20 @@ int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t 
 int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
                       int64_t C_out, const int64_t k_dims[4], float* y, int dtype, void* stream);
 
-/* Synchronise `stream`, then read and clear the handle's device status word.
+/* Synchronise `stream`, then read and clear the handle's device status word.  This is
+ * the wait of "Learning to develop for GPU with GEMM as the example", section "Writing a
+ * GPU implementation of matrix multiplication" (its part on launching the kernel: the host
+ * waits on an event for the enqueued kernel), extended with the kernel's own report.
  * Returns GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a kernel launched through this
  * handle gave up on a bounded wait since the last call (its output is then invalid),
  * or GEMM_ERR_CUDA if the stream reports an error. */
 int gemm_get_device_status(gemm_handle_t h, void* stream);
 
 /* Tuning and test options (see GEMM_OPT_*).  Values outside the documented range are
- * rejected with GEMM_ERR_INVALID_ARG.  Defaults are restored by passing 0. */
+ * rejected with GEMM_ERR_INVALID_ARG.  Defaults are restored by passing 0.
+ * The choices "Three X: large convolutions in PyTorch for training", section "How to
+ * call a convolution in the CUTLASS library", makes when it builds the operation's type
+ * (which tile iterator, which epilogue), made here at run time on a handle. */
 typedef enum {
     GEMM_OPT_F32_KERNEL = 1, /* 0 auto, 1 tiled 128x256 FFMA, 2 tiled 64x128 FFMA, 3 skinny streaming from
                                 registers (M<=32), 4 skinny streaming through a TMA ring (M<=32; B 16-byte
@@ -231,7 +257,10 @@ typedef enum {
 int gemm_set_option(gemm_handle_t h, int option, int64_t value);
 
 /* Number of kernels launched through this handle since it was created (a cumulative
- * count kept on the host; -1 for a NULL handle).  Zero-size calls launch nothing. */
+ * count kept on the host; -1 for a NULL handle).  Zero-size calls launch nothing.
+ * It counts the kernel enqueues of "Learning to develop for GPU with GEMM as the
+ * example", section "Writing a GPU implementation of matrix multiplication" (its part on
+ * launching the kernel). */
 int64_t gemm_launch_count(gemm_handle_t h);
 
 /* fp32 C = A . B for M <= 32 (the skinny streaming kernel) WITHOUT ALLOCATING.
@@ -267,7 +296,10 @@ int gemm_run_f32_skinny_noalloc(int64_t M, int64_t N, int64_t K, const float* A,
                                 const float* B, int64_t ldb, float* C, int64_t ldc, int split_k,
                                 void* stream);
 
-/* Static string describing a status code. */
+/* Static string describing a status code: the outcome of a step of the host program of
+ * "Learning to develop for GPU with GEMM as the example", section "Writing a GPU
+ * implementation of matrix multiplication" (device set-up, argument checks, the enqueue,
+ * the wait). */
 const char* gemm_status_string(int status);
 
 #ifdef __cplusplus

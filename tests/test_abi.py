@@ -93,3 +93,30 @@ def test_no_multicast_bulk_copy_in_the_sources():
         text = open(os.path.join(csrc, name)).read()
         for stmt in re.findall(r"cp\.(?:async|reduce\.async)\.bulk[^;\"]*", text):
             assert "multicast" not in stmt, (name, stmt)
+
+
+def declarations_with_comments():
+    """(function name, the comment block right before its declaration) for every function
+    the header declares."""
+    text = open(HEADER).read()
+    # drop type definitions with braces (and the comments inside them), keeping the comment
+    # in front: a declaration may follow the option enum its comment also describes
+    text = re.sub(r"typedef\s+(?:enum|struct)[^{;]*\{.*?\}\s*\w+\s*;", "", text, flags=re.S)
+    out = []
+    for m in re.finditer(r"/\*((?:(?!\*/).)*)\*/\s*(typedef[^;]*;\s*)?(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.S):
+        if m.group(2):
+            continue  # the comment belongs to a type
+        out.append((m.group(3), m.group(1)))
+    return out
+
+
+def test_every_declaration_cites_its_passage():
+    """Each entry point's comment names the page and the section it implements, or says
+    that the pages have no counterpart."""
+    found = dict(declarations_with_comments())
+    assert sorted(found) == declared_functions()
+    for name, comment in found.items():
+        flat = " ".join(re.sub(r"^\s*\*", "", line) for line in comment.splitlines())
+        flat = " ".join(flat.split())
+        cited = re.search(r'"[^"]+", sections? "[^"]+"', flat) or re.search(r'"[^"]+" sections? "[^"]+"', flat)
+        assert cited or "no counterpart" in flat, name
