@@ -279,7 +279,10 @@ int64_t gemm_launch_count(gemm_handle_t h);
  * allocating library routine.
  *   - The FIRST call on each device looks up that array's device address
  *     (cudaGetSymbolAddress, which may load the library's device code); make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The address is cached with the unique ID
+ *     of the context it was taken in, and a call made under another context of that
+ *     device (after cudaDeviceReset, or with a context the caller made current) looks
+ *     it up again: such a call is a first call too.
  *   - All calls share the one array and it keeps the last call's contents: two
  *     calls that can run at the same time on the GPU (different streams, or
  *     different host threads) race on it and both results are then undefined.
@@ -289,8 +292,9 @@ int64_t gemm_launch_count(gemm_handle_t h);
  * GEMM_OPT_F32_KERNEL = 3.  Arguments as in gemm_run with dtype GEMM_F32; split_k = 0
  * picks the split gemm_run picks for that kernel (results are then bit-identical to
  * gemm_run with that option; gemm_run's default TMA-fed kernel agrees within fp32
- * rounding), 1..1024 forces one.  Errors: GEMM_ERR_INVALID_ARG for bad arguments, GEMM_ERR_UNSUPPORTED
- * for M > 32, for a device that is not sm_103, or when split_k * M * N exceeds the
+ * rounding), 1..1024 forces one.  Errors: GEMM_ERR_INVALID_ARG for bad arguments (gemm_run's
+ * checks), GEMM_ERR_UNSUPPORTED for M > 32, for sizes beyond the kernels' 32-bit indexing
+ * (as gemm_run), for a device that is not sm_103, or when split * M * N exceeds the
  * 8,388,608-float scratch array (the size limit); nothing is written then. */
 int gemm_run_f32_skinny_noalloc(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                 const float* B, int64_t ldb, float* C, int64_t ldc, int split_k,

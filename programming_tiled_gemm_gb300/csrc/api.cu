@@ -16,6 +16,36 @@
 
 using namespace gemm_gb300;
 
+namespace gemm_gb300 {
+
+int check_product_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                       const void* C, int64_t ldc)
+{
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (!A || !B) return GEMM_ERR_INVALID_ARG;
+        if (lda < K || ldb < N) return GEMM_ERR_INVALID_ARG;
+    }
+    // the largest element offsets must fit in int64 (they always do for real memory,
+    // but reject nonsense before it reaches a kernel)
+    const int64_t lim = (int64_t)1 << 46;
+    if (M > lim / (ldc > 0 ? ldc : 1) || (K > 0 && (M > lim / lda || K > lim / ldb)))
+        return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+// Every kernel indexes with 32-bit sizes and leading dimensions: larger ones are refused
+// before anything is allocated or launched.
+bool beyond_kernel_limits(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc)
+{
+    constexpr int64_t kLim32 = 0x7fffffffLL - 1024;
+    return M > kLim32 || N > kLim32 || K > kLim32 || ldc > kLim32 || (K > 0 && (lda > kLim32 || ldb > kLim32));
+}
+
+}  // namespace gemm_gb300
+
 struct gemm_ctx {
     int device = 0;
     int num_sms = 0;
@@ -91,26 +121,7 @@ int check_common(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A
     if (!h) return GEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (dtype != GEMM_F32 && dtype != GEMM_BF16 && dtype != GEMM_F16) return GEMM_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return GEMM_OK;
-    if (!C || ldc < N) return GEMM_ERR_INVALID_ARG;
-    if (K > 0) {
-        if (!A || !B) return GEMM_ERR_INVALID_ARG;
-        if (lda < K || ldb < N) return GEMM_ERR_INVALID_ARG;
-    }
-    // the largest element offsets must fit in int64 (they always do for real memory,
-    // but reject nonsense before it reaches a kernel)
-    const int64_t lim = (int64_t)1 << 46;
-    if (M > lim / (ldc > 0 ? ldc : 1) || (K > 0 && (M > lim / lda || K > lim / ldb)))
-        return GEMM_ERR_INVALID_ARG;
-    return GEMM_OK;
-}
-
-// Every kernel indexes with 32-bit sizes and leading dimensions: larger ones are refused
-// before anything is allocated or launched.
-bool beyond_kernel_limits(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc)
-{
-    constexpr int64_t kLim32 = 0x7fffffffLL - 1024;
-    return M > kLim32 || N > kLim32 || K > kLim32 || ldc > kLim32 || (K > 0 && (lda > kLim32 || ldb > kLim32));
+    return check_product_args(M, N, K, A, lda, B, ldb, C, ldc);
 }
 
 int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)

@@ -31,6 +31,14 @@ struct Epilogue {
 cudaError_t launch_epilogue(const float* P, int64_t ldp, void* C, int64_t ldc, int64_t M, int64_t N,
                             const Epilogue& epi, int num_sms, cudaStream_t stream);
 
+// Argument checks every product entry point shares (sizes, pointers, leading dimensions
+// and the int64 element-offset range).  GEMM_OK, or GEMM_ERR_INVALID_ARG.  M == 0 or
+// N == 0 passes (nothing is done).
+int check_product_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                       const void* C, int64_t ldc);
+// True when a size or leading dimension is beyond the kernels' 32-bit indexing.
+bool beyond_kernel_limits(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc);
+
 struct F32Args {
     int64_t M, N, K;
     const float* A;

@@ -120,3 +120,15 @@ def test_every_declaration_cites_its_passage():
         flat = " ".join(flat.split())
         cited = re.search(r'"[^"]+", sections? "[^"]+"', flat) or re.search(r'"[^"]+" sections? "[^"]+"', flat)
         assert cited or "no counterpart" in flat, name
+
+
+def test_noalloc_entry_point_checks_sizes_before_touching_cuda(pkg):
+    """The allocation-free entry point applies gemm_run's argument and size checks before
+    any CUDA call (the pointers below are never dereferenced)."""
+    lib = pkg.library()
+    big, huge, p = 1 << 40, 1 << 62, 256
+    assert lib.gemm_run_f32_skinny_noalloc(16, big, 64, p, 64, p, big, p, big, 0, None) == pkg.GEMM_ERR_UNSUPPORTED
+    assert lib.gemm_run_f32_skinny_noalloc(16, 256, 64, p, 64, p, huge, p, 256, 0, None) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_run_f32_skinny_noalloc(33, 256, 64, p, 64, p, 256, p, 256, 0, None) == pkg.GEMM_ERR_UNSUPPORTED
+    assert lib.gemm_run_f32_skinny_noalloc(16, 256, 64, p, 63, p, 256, p, 256, 0, None) == pkg.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_run_f32_skinny_noalloc(16, 256, 64, p, 64, p, 256, p, 256, 2000, None) == pkg.GEMM_ERR_INVALID_ARG

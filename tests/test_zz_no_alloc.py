@@ -105,3 +105,53 @@ def test_size_limit_and_argument_errors(g):
     assert lib.gemm_run_f32_skinny_noalloc(4, 4, 4, None, 4, None, 4, None, 4, 0, None) == g.GEMM_ERR_INVALID_ARG
     assert lib.gemm_run_f32_skinny_noalloc(4, 4, 4, A.data_ptr(), 3, B.data_ptr(), 16384, C.data_ptr(), 16384,
                                            0, None) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_leftover_scratch_from_a_larger_split_never_reaches_the_sum(g):
+    """A call with a large split x M x N layout fills the shared scratch array with NaN
+    partial sums (its inputs hold NaNs); the next call, on the same stream, uses a smaller
+    layout over the same array and must still equal gemm_run: every partial sum it adds
+    was written by itself."""
+    dev = torch.device("cuda")
+    # shape X: split 9, 24 x 8000 -> 1.73 Mi floats of partials, all NaN
+    Ax = torch.full((24, 900), float("nan"), device=dev)
+    Bx = torch.ones((900, 8000), device=dev)
+    Cx = torch.empty((24, 8000), device=dev)
+    assert noalloc(g, Ax, Bx, Cx, split_k=9) == g.GEMM_OK
+    # shape Y: split 3, 7 x 3001 -> a different slice stride over the same array
+    A, B = si.gemm_operands(7, 3001, 1500, seed=23)
+    Ad, Bd = A.to(dev), B.to(dev)
+    ref_lib = g.Gemm(0)
+    ref_lib.set_option(g.GEMM_OPT_SPLIT_K, 3)
+    ref_lib.set_option(g.GEMM_OPT_F32_KERNEL, 3)
+    ref = ref_lib.matmul(Ad, Bd)
+    for _ in range(2):
+        Cy = torch.full((7, 3001), float("nan"), device=dev)
+        assert noalloc(g, Ad, Bd, Cy, split_k=3) == g.GEMM_OK
+        torch.cuda.synchronize()
+        assert torch.isnan(Cx).all()  # the first call really left NaNs behind
+        assert torch.isfinite(Cy).all()
+        assert torch.equal(Cy, ref)
+        assert (Cy - ref).abs().max().item() <= 1e-5 * math.sqrt(1500)
+        assert noalloc(g, Ax, Bx, Cx, split_k=9) == g.GEMM_OK  # NaNs again before the repeat
+    ref_lib.close()
+
+
+def test_sizes_beyond_the_kernels_limits_are_refused_before_any_launch(g):
+    """The entry point applies gemm_run's checks: 32-bit kernel limits (unsupported) and
+    the element-offset range (invalid), and compares the scratch need without
+    overflowing."""
+    dev = torch.device("cuda")
+    A = torch.ones((16, 64), device=dev)
+    B = torch.ones((64, 256), device=dev)
+    C = torch.empty((16, 256), device=dev)
+    lib = g.library()
+    big = 1 << 40  # N far beyond 32-bit indexing; split * M * N would not overflow int64 here
+    assert lib.gemm_run_f32_skinny_noalloc(16, big, 64, A.data_ptr(), 64, B.data_ptr(), big, C.data_ptr(), big,
+                                           0, None) == g.GEMM_ERR_UNSUPPORTED
+    huge = 1 << 62  # leading dimensions whose offsets leave the int64 range
+    assert lib.gemm_run_f32_skinny_noalloc(16, 256, 64, A.data_ptr(), 64, B.data_ptr(), huge, C.data_ptr(), 256,
+                                           0, None) == g.GEMM_ERR_INVALID_ARG
+    assert noalloc(g, A, B, C) == g.GEMM_OK  # a valid call still runs after the refusals
+    torch.cuda.synchronize()
+    assert torch.equal(C, torch.full_like(C, 64.0))
