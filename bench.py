@@ -32,11 +32,10 @@ sys.path.insert(0, ROOT)
 METRIC = "GEMM TFLOP/s (2MNK/device time) & % of GB300 peak, bf16 8192³ and fp32 4096³"
 DEFAULT_WORKLOADS = ["bf16_8192", "f32_4096"]
 EXTRA_WORKLOADS = ["f32_skinny", "conv4d"]
-SM_COUNT_GB300 = 152
 FP32_LANES_PER_SM = 128
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
 L2_FLUSH_BYTES = 512 << 20
-WARM_REPS = 10  # back-to-back repetitions per workload for the warm-L2 context numbers
+CLOCK_WINDOW_S = 1.5  # back-to-back run per workload with the clock sampler on (warm-L2 context numbers)
 
 
 def parse():
@@ -71,9 +70,9 @@ def load_peaks():
     return dict(FALLBACK), "fallback"
 
 
-def fp32_simt_peak_tflops(sm_mhz: float) -> float:
-    """FP32 FFMA peak: SMs x 128 lanes x 2 flop x clock."""
-    return SM_COUNT_GB300 * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+def fp32_simt_peak_tflops(sm_mhz: float, sms: int) -> float:
+    """FP32 FFMA peak: SMs (queried from the device) x 128 lanes x 2 flop x clock."""
+    return sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
 
 
 # ------------------------------------------------------------------ clock sampling
@@ -103,6 +102,7 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
+        self.rows = None
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -110,36 +110,43 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.fh.close()
+            self.rows = []
+            with open(self.path) as fh:
+                for r in csv.reader(fh):
+                    if len(r) >= 9:
+                        self.rows.append([c.strip() for c in r])
+        if self.path and os.path.exists(self.path):
+            os.unlink(self.path)
 
     def summary(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        rows = []
-        with open(self.path) as fh:
-            for r in csv.reader(fh):
-                if len(r) >= 9:
-                    rows.append([c.strip() for c in r])
-        os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return summarize_clocks(self.rows)
 
-        def num(s):
-            try:
-                return float(s)
-            except ValueError:
-                return None
-        smax = max((num(r[2]) or 0) for r in rows)
-        busy = [r for r in rows if (num(r[3]) or 0) > 250.0] or rows  # power draw marks load
-        clocks = [num(r[1]) for r in busy if num(r[1]) is not None]
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in busy:
-            for name, v in zip(names, r[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(clocks) if clocks else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(busy),
-                "power_w_max": max((num(r[3]) or 0) for r in rows)}
+
+def summarize_clocks(rows):
+    """Median SM clock and throttle reasons over the samples taken under load (power
+    draw above 250 W), from nvidia-smi rows; rows None = no sampler."""
+    if rows is None:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+    def num(v):
+        try:
+            return float(v)
+        except ValueError:
+            return None
+    smax = max((num(r[2]) or 0) for r in rows)
+    busy = [r for r in rows if (num(r[3]) or 0) > 250.0] or rows  # power draw marks load
+    clocks = [num(r[1]) for r in busy if num(r[1]) is not None]
+    reasons = set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in busy:
+        for name, v in zip(names, r[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(clocks) if clocks else None, "sm_max_mhz": smax,
+            "reasons": sorted(reasons), "samples": len(busy),
+            "power_w_max": max((num(r[3]) or 0) for r in rows)}
 
 
 def reduce_max(value: float, dist_mod, device) -> float:
@@ -229,10 +236,12 @@ def run_ours(args, rank, world, local_rank):
 
     def run_op(op):
         w, Ad, Bd, Cd = op
+        torch.cuda.nvtx.range_push(w.name)  # lets a profiler's range filter pick one product
         if w.kind == "conv4d":
             lib.conv4d_implicit(Ad, Bd, out=Cd)  # implicit GEMM: y = W . col(x), no column matrix
         else:
             lib.matmul(Ad, Bd, out=Cd)
+        torch.cuda.nvtx.range_pop()
 
     for _ in range(args.warmup):
         for op in ops:
@@ -263,41 +272,58 @@ def run_ours(args, rank, world, local_rank):
         step_ms = [evs[s][0].elapsed_time(evs[s][-1]) for s in range(args.steps)]
         return step_ms, per_op, wall, launches
 
+    def clock_windows():
+        """Each workload back to back (no flush) for about CLOCK_WINDOW_S with the clock
+        sampler on: its warm-L2 time and the SM clock the GPU holds under that load
+        (the timed region itself is too short for a 100 ms sampler to see)."""
+        res = []
+        for op in ops:
+            run_op(op)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run_op(op)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            reps = max(10, int(CLOCK_WINDOW_S * 1e3 / max(e0.elapsed_time(e1), 1e-3)))
+            with ClockSampler(local_rank) as cw:
+                e0.record(stream)
+                for _ in range(reps):
+                    run_op(op)
+                e1.record(stream)
+                torch.cuda.synchronize()
+            res.append((e0.elapsed_time(e1) / reps, reps, cw.rows))
+        return res
+
     with ClockSampler(local_rank) as cs:
         step_ms, per_op, wall, launches = timed_region()
-    clocks = cs.summary()
+    windows = clock_windows()
     remeasured = False
+
+    def all_clocks(timed_rows, wins):
+        rows = None if timed_rows is None else list(timed_rows) + [r for *_, rw in wins for r in (rw or [])]
+        return summarize_clocks(rows)
+    clocks = all_clocks(cs.rows, windows)
     if clocks_rejected(clocks):
         with ClockSampler(local_rank) as cs:
             step_ms, per_op, wall, launches = timed_region()
-        clocks = cs.summary()
+        windows = clock_windows()
+        clocks = all_clocks(cs.rows, windows)
         remeasured = True
+    clocks["timed_region"] = summarize_clocks(cs.rows)
     if lib.device_status() != 0:
         raise RuntimeError("device status error in the timed region")
 
     flops_step = sum(op[0].flops for op in ops)
     value, ms_step = aggregate(flops_step, statistics.mean(step_ms), world, pg, dev)
 
-    # warm-L2 times for context: repetitions back to back, no flush in between (after the
-    # timed region; not part of `value`)
-    warm_ms = []
-    for op in ops:
-        run_op(op)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(WARM_REPS):
-            run_op(op)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        warm_ms.append(e0.elapsed_time(e1) / WARM_REPS)
-
     peaks, peak_src = load_peaks()
-    sm_mhz = clocks.get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
-    fp32_peak = fp32_simt_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak = fp32_simt_peak_tflops(peaks.get("sm_max_mhz", 2070.0), sms)
     per = {}
     kernels = []
-    for (w, *_), times, wms in zip(ops, per_op, warm_ms):
+    for (w, *_), times, (wms, wreps, wrows) in zip(ops, per_op, windows):
         ms = statistics.mean(times)
+        wclk = summarize_clocks(wrows)
         tflops = w.flops / (ms * 1e-3) / 1e12
         if w.dtype == "bf16":
             peak, bound, kname = peaks["bf16_tflops"], "tensor", "tc_gemm"
@@ -309,9 +335,17 @@ def run_ours(args, rank, world, local_rank):
             peak, bound, kname = fp32_peak, "alu", "ffma_tiled"
         entry = {"ms": round(ms, 4), "tflops": round(tflops, 2), "peak_tflops": round(peak, 1),
                  "frac": round(tflops / peak, 4), "flops": w.flops, "input_sha256": shas[w.name],
-                 "warm_ms": round(wms, 4), "warm_tflops": round(w.flops / (wms * 1e-3) / 1e12, 2)}
+                 "warm_ms": round(wms, 4), "warm_tflops": round(w.flops / (wms * 1e-3) / 1e12, 2),
+                 "clock_window": {"reps": wreps, "seconds": round(wms * wreps * 1e-3, 2),
+                                  "sm_mhz": wclk.get("sm_mhz"), "samples": wclk.get("samples"),
+                                  "reasons": wclk.get("reasons")}}
+        wmhz = wclk.get("sm_mhz")
+        if wmhz:
+            # the kernel time scaled to cycles: time x the SM clock held under this load
+            entry["ms_x_sm_ghz"] = round(ms * wmhz / 1e3, 4)
         if w.dtype != "bf16":
-            entry["frac_at_median_clock"] = round(tflops / fp32_simt_peak_tflops(sm_mhz), 4)
+            if wmhz:
+                entry["frac_at_median_clock"] = round(tflops / fp32_simt_peak_tflops(wmhz, sms), 4)
         else:
             entry["frac_of_sustained"] = round(tflops / peaks.get("bf16_tflops_sustained", peak), 4)
         per[w.name] = entry
@@ -321,8 +355,9 @@ def run_ours(args, rank, world, local_rank):
     roofline = {"kernel": kname, "workload": w_dom.name, "bound": bound, "achieved": round(tflops, 2),
                 "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                 "peak_source": ("of measured" if (bound == "tensor" and peak_src == "measured") else
-                                "derived: 152 SMs x 128 FP32 lanes x 2 flop x %.0f MHz (max SM clock)"
-                                % peaks.get("sm_max_mhz", 2070.0) if bound == "alu" else "of fallback"),
+                                "derived: %d SMs (queried from the device) x 128 FP32 lanes x 2 flop x %.0f MHz "
+                                "(max SM clock)" % (sms, peaks.get("sm_max_mhz", 2070.0)) if bound == "alu"
+                                else "of fallback"),
                 "traffic": recorded_traffic(kname, w_dom.flops)}
     rooflines = [{"kernel": k[2], "workload": k[1].name, "bound": k[3], "achieved": round(k[5], 2),
                   "peak": round(k[4], 1), "unit": "TFLOP/s", "frac": round(k[5] / k[4], 4),

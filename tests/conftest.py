@@ -28,3 +28,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.hookimpl(hookwrapper=True)
+def pytest_runtest_call(item):
+    """Each GPU test runs inside an NVTX range named after it, so that a profiler's range
+    filter (ncu --nvtx --nvtx-include) can pick one test's products out of a session."""
+    nvtx = None
+    if "gpu" in item.keywords and _has_gpu():
+        import torch
+        nvtx = torch.cuda.nvtx
+        nvtx.range_push(item.nodeid)
+    try:
+        yield
+    finally:
+        if nvtx is not None:
+            nvtx.range_pop()

@@ -69,3 +69,26 @@ def test_reference_arm_prints_the_contract_line():
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["e2e"]["value"] == rec["value"]
     assert rec["steps"] == 2 and rec["warmup"] == 3
+
+
+def test_clock_summary_counts_loaded_samples_and_reasons():
+    sys.path.insert(0, ROOT)
+    import bench
+    idle = ["0", "1980", "2070", "120.5", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]
+    busy = ["0", "1750", "2070", "1350.0", "0x4", "Not Active", "Not Active", "Not Active", "Active"]
+    fast = ["0", "2070", "2070", "900.0", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]
+    c = bench.summarize_clocks([idle, busy, busy, fast, idle])
+    assert c["samples"] == 3 and c["sm_mhz"] == 1750.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"] and not bench.clocks_rejected(c)
+    hot = list(busy)
+    hot[7] = "Active"
+    assert bench.clocks_rejected(bench.summarize_clocks([hot]))
+    assert bench.summarize_clocks(None)["samples"] == 0
+    assert bench.summarize_clocks([])["samples"] == 0
+
+
+def test_fp32_peak_uses_the_given_sm_count():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert abs(bench.fp32_simt_peak_tflops(2070.0, 152) - 80.547) < 1e-3
+    assert abs(bench.fp32_simt_peak_tflops(2070.0, 76) - 80.547 / 2) < 1e-3
