@@ -230,9 +230,12 @@ int gemm_get_device_status(gemm_handle_t h, void* stream);
  * call a convolution in the CUTLASS library", makes when it builds the operation's type
  * (which tile iterator, which epilogue), made here at run time on a handle. */
 typedef enum {
-    GEMM_OPT_F32_KERNEL = 1, /* 0 auto, 1 tiled 128x256 FFMA, 2 tiled 64x128 FFMA, 3 skinny streaming from
-                                registers (M<=32), 4 skinny streaming through a TMA ring (M<=32; B 16-byte
-                                aligned with ldb % 4 == 0, else GEMM_ERR_ALIGNMENT) */
+    GEMM_OPT_F32_KERNEL = 1, /* 0 auto, 1 tiled 128x256 FFMA (one launch per wave kind), 2 tiled 64x128 FFMA,
+                                3 skinny streaming from registers (M<=32), 4 skinny streaming through a TMA
+                                ring (M<=32; B 16-byte aligned with ldb % 4 == 0, else GEMM_ERR_ALIGNMENT),
+                                5 persistent 128x256 FFMA fed by TMA, one launch per product (A and B
+                                16-byte aligned with lda, ldb % 4 == 0, else GEMM_ERR_ALIGNMENT).  Auto:
+                                M<=32 skinny (4, else 3), M<=64 2, else 5 when its alignment holds, else 1 */
     GEMM_OPT_SPLIT_K = 2,    /* 0 auto, else the split-K factor for fp32 kernels (1..1024) */
     GEMM_OPT_WAIT_LIMIT_US = 3, /* 0 default (2 s), else the bounded-wait limit of device waits in microseconds */
     GEMM_OPT_TC_CHUNK = 4,      /* 0 default (16), else the tensor-core accumulation chunk in 64-wide k-blocks
@@ -245,7 +248,8 @@ typedef enum {
                                    128x256 tile, 2 a pair of CTAs (cluster of two) per 256x256 tile.  Any
                                    other value (3 included) is GEMM_ERR_INVALID_ARG */
     GEMM_OPT_TEST_STALL = 6,    /* test hook for failure detection, 0 (default) or 1: the kernels with
-                                   bounded waits (tensor-core GEMMs and convolution, TMA skinny GEMM) first wait on a
+                                   bounded waits (tensor-core GEMMs and convolution, TMA skinny GEMM, persistent
+                                   fp32 GEMM) first wait on a
                                    barrier nothing arrives on; the wait runs out after the wait limit, the
                                    kernel drains its copies and MMAs, frees its tensor memory, returns,
                                    and gemm_get_device_status reports GEMM_ERR_DEVICE_TIMEOUT.  C is not

@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libgemm_gb300.so")
 
-SOURCES = ["api.cu", "ffma.cu", "skinny.cu", "skinny_tma.cu", "im2col.cu", "conv_implicit.cu", "conv_tc.cu", "tc_gemm.cu",
+SOURCES = ["api.cu", "ffma.cu", "ffma_tma.cu", "skinny.cu", "skinny_tma.cu", "im2col.cu", "conv_implicit.cu", "conv_tc.cu", "tc_gemm.cu",
            "skinny_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

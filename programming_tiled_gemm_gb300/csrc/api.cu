@@ -55,6 +55,9 @@ struct gemm_ctx {
     unsigned long long* tc_counters = nullptr;  // last-wave split counters of the tensor-core GEMM
     size_t tc_counters_bytes = 0;
     unsigned tc_seq = 0;  // tag of the last split tensor-core launch
+    unsigned long long* f32_counters = nullptr;  // K-slice counters of the persistent fp32 GEMM
+    size_t f32_counters_bytes = 0;
+    unsigned f32_seq = 0;  // tag of the last split persistent fp32 launch
     void* host_stage = nullptr;  // gemm_run_host(_batch) device copies of A, B and C
     size_t host_stage_bytes = 0;
     float* product = nullptr;  // fp32 product for the generalised epilogue of fp32 inputs
@@ -124,12 +127,45 @@ int check_common(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A
     return check_product_args(M, N, K, A, lda, B, ldb, C, ldc);
 }
 
+// Tagged arrival counters: a launch trusts only counts carrying its own tag, so the buffer
+// is zeroed only when (re)allocated and when the tag wraps.
+int tagged_counters(unsigned long long** buf, size_t* have, unsigned* seq, int64_t n, cudaStream_t s)
+{
+    const size_t bytes = (size_t)n * sizeof(unsigned long long);
+    const bool fresh = !*buf || *have < bytes;
+    int rc = ensure_buffer(reinterpret_cast<void**>(buf), have, bytes);
+    if (rc != GEMM_OK) return rc;
+    if (++*seq == 0) *seq = 1;
+    if ((fresh || *seq == 1) && cudaMemsetAsync(*buf, 0, *have, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
 int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)
 {
     int kernel = h->opt_f32_kernel;
-    if (kernel == 0) kernel = (a.M <= 32) ? (skinny_tma_supported(a) ? 4 : 3) : (a.M <= 64 ? 2 : 1);
+    if (kernel == 0)
+        kernel = (a.M <= 32) ? (skinny_tma_supported(a) ? 4 : 3)
+                 : (a.M <= 64) ? 2
+                               : (ffma_persistent_supported(a) ? 5 : 1);
     if ((kernel == 3 || kernel == 4) && a.M > 32) return GEMM_ERR_UNSUPPORTED;
     if (kernel == 4 && !skinny_tma_supported(a)) return GEMM_ERR_ALIGNMENT;
+    if (kernel == 5) {
+        if (!ffma_persistent_supported(a)) return GEMM_ERR_ALIGNMENT;
+        const FfmaPlan pl = ffma_persistent_plan(a, h->opt_split_k, h->num_sms);
+        if (pl.split > 1) {
+            int rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes,
+                                   (size_t)pl.ws_floats * sizeof(float));
+            if (rc != GEMM_OK) return rc;
+        }
+        int rc = tagged_counters(&h->f32_counters, &h->f32_counters_bytes, &h->f32_seq, pl.counters, stream);
+        if (rc != GEMM_OK) return rc;
+        const uint32_t seq = h->f32_seq;
+        int n = 0;
+        cudaError_t e = launch_ffma_persistent(a, pl, h->workspace, h->f32_counters, seq, h->num_sms, h->d_status,
+                                               h->wait_limit_ns, h->opt_test_stall, stream, &n);
+        h->launches += n;
+        return from_cuda(e);
+    }
     int split = h->opt_split_k;
     if (split == 0)
         split = (kernel == 4)   ? skinny_tma_auto_split(a, h->num_sms)
@@ -207,6 +243,7 @@ int gemm_destroy(gemm_handle_t h)
     if (h->d_status) cudaFree(h->d_status);
     if (h->workspace) cudaFree(h->workspace);
     if (h->tc_counters) cudaFree(h->tc_counters);
+    if (h->f32_counters) cudaFree(h->f32_counters);
     if (h->product) cudaFree(h->product);
     if (h->host_stage) cudaFree(h->host_stage);
     delete h;
@@ -218,7 +255,7 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     if (!h) return GEMM_ERR_INVALID_ARG;
     switch (option) {
     case GEMM_OPT_F32_KERNEL:
-        if (value < 0 || value > 4) return GEMM_ERR_INVALID_ARG;
+        if (value < 0 || value > 5) return GEMM_ERR_INVALID_ARG;
         h->opt_f32_kernel = (int)value;
         return GEMM_OK;
     case GEMM_OPT_SPLIT_K:

@@ -55,6 +55,25 @@ struct F32Args {
 cudaError_t launch_ffma_tiled(const F32Args& a, int variant, int split, float* workspace,
                               int num_sms, cudaStream_t stream, int* launches);
 
+// fp32 GEMM as one persistent launch fed by TMA (128 x 256 x 32 tiles, grouped raster,
+// items handed out dynamically):
+// a last, partial wave of tiles runs as K slices whose partial tiles the slice that
+// finishes last adds in slice order.  Needs 16-byte aligned A and B with lda, ldb % 4 == 0.
+struct FfmaPlan {
+    int64_t tiles = 0, k_tiles = 0;
+    int64_t split_first = 0;   // tiles [split_first, tiles) are cut into `split` K slices
+    int split = 1;
+    int64_t kt_per_slice = 0;  // 32-deep k-tiles per slice
+    int64_t ws_floats = 0;     // partial-tile workspace the slices need
+    int64_t counters = 0;      // tagged 64-bit counters: one per split tile, then the item counter
+};
+bool ffma_persistent_supported(const F32Args& a);
+// split_opt > 0 forces that split on every tile.
+FfmaPlan ffma_persistent_plan(const F32Args& a, int split_opt, int num_sms);
+cudaError_t launch_ffma_persistent(const F32Args& a, const FfmaPlan& plan, float* ws, unsigned long long* cnt,
+                                   uint32_t seq, int num_sms, int* dev_status, uint64_t limit_ns, int test_stall,
+                                   cudaStream_t stream, int* launches);
+
 // fp32 skinny streaming GEMM for M <= 32: B is read once, straight into registers.
 cudaError_t launch_skinny(const F32Args& a, int split, float* workspace, int num_sms,
                           cudaStream_t stream, int* launches);

@@ -3,10 +3,11 @@
 Tolerances (max |C - C_ref| over the compared entries):
   * integer-valued inputs in [-4, 4]: exact (every partial sum is an integer below 2^24);
   * uniform[-1, 1] inputs: 1e-5 * sqrt(K).
-Kernels: the 128x256 and 64x128 tiled FFMA kernels (with and without split-K) and the two
-skinny kernels (B streamed through registers, or through a TMA ring in shared memory),
-each forced on shapes with ragged tails, padded leading dimensions and guard bands
-around C.
+Kernels: the 128x256 and 64x128 tiled FFMA kernels (with and without split-K), the
+persistent TMA-fed 128x256 kernel (one launch; K slices added by the slice that finishes
+last) and the two skinny kernels (B streamed through registers, or through a TMA ring in
+shared memory), each forced on shapes with ragged tails, padded leading dimensions and
+guard bands around C.
 """
 import math
 
@@ -65,7 +66,13 @@ def ref_of(A, B):
     return oracle.gemm(A.numpy(), B.numpy())
 
 
-KERNELS = [(1, 0), (1, 3), (2, 0), (2, 2), (3, 0), (3, 5), (4, 0), (4, 5)]  # (kernel, split-K: 0 = auto)
+KERNELS = [(1, 0), (1, 3), (2, 0), (2, 2), (3, 0), (3, 5), (4, 0), (4, 5), (5, 0), (5, 3)]  # (kernel, split-K: 0 = auto)
+TMA_FED = (4, 5)  # kernels that need 16-byte rows of B (5: and of A)
+
+
+def pad_to_16_bytes(n):
+    """Padding that makes a row of n floats a multiple of 16 bytes (plus 4 floats of slack)."""
+    return (4 - n % 4) % 4 + 4
 
 
 @pytest.mark.parametrize("kernel,split", KERNELS)
@@ -77,8 +84,9 @@ def test_integer_inputs_are_exact(lib, kernel, split, M, N, K):
     lib.set_option(g.GEMM_OPT_F32_KERNEL, kernel)
     lib.set_option(g.GEMM_OPT_SPLIT_K, split)
     A, B = si.integer_copy(M, N, K, seed=M * 1000 + N + K)
-    # the TMA-fed kernel needs 16-byte B rows: pad ldb to a multiple of 4 floats
-    got = run_padded(lib, A, B, pad_a=3, pad_b=(4 - N % 4) % 4 + 4 if kernel == 4 else 5, pad_c=1)
+    # the TMA-fed kernels need 16-byte rows: pad ldb (and lda) to a multiple of 4 floats
+    got = run_padded(lib, A, B, pad_a=pad_to_16_bytes(K) if kernel == 5 else 3,
+                     pad_b=pad_to_16_bytes(N) if kernel in TMA_FED else 5, pad_c=1)
     assert np.array_equal(got, ref_of(A, B))
 
 
@@ -91,7 +99,7 @@ def test_uniform_inputs_within_tolerance(lib, kernel, split, M, N, K):
     lib.set_option(g.GEMM_OPT_F32_KERNEL, kernel)
     lib.set_option(g.GEMM_OPT_SPLIT_K, split)
     A, B = si.gemm_operands(M, N, K, seed=5)
-    got = run_padded(lib, A, B, pad_b=(4 - N % 4) % 4 + 4)
+    got = run_padded(lib, A, B, pad_a=pad_to_16_bytes(K) if kernel == 5 else 0, pad_b=pad_to_16_bytes(N))
     assert np.abs(got - ref_of(A, B)).max() <= 1e-5 * math.sqrt(K)
 
 
@@ -173,6 +181,8 @@ def last_wave_plan(interior, slots, K):
 def test_last_wave_tiles_split_along_K(lib, M, N):
     # 13 x 13 = 169 interior 128 x 256 tiles: on 152 SMs the 17 tiles of the last wave run
     # cut into K slices whose partial tiles are summed in a separate fixed-order pass
+    import programming_tiled_gemm_gb300 as g
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, 1)
     K = 2048
     slots = torch.cuda.get_device_properties(0).multi_processor_count
     rem, rs = last_wave_plan((M // 128) * (N // 256), slots, K)
@@ -210,7 +220,7 @@ def test_results_are_deterministic(lib):
     import programming_tiled_gemm_gb300 as g
     A, B = si.gemm_operands(24, 3000, 5000, seed=9)
     Ad, Bd = A.cuda(), B.cuda()
-    for kernel in (1, 2, 3, 4):
+    for kernel in (1, 2, 3, 4, 5):
         lib.set_option(g.GEMM_OPT_F32_KERNEL, kernel)
         lib.set_option(g.GEMM_OPT_SPLIT_K, 7)
         c1 = lib.matmul(Ad, Bd).clone()
@@ -272,3 +282,89 @@ def test_host_buffer_entry_point(lib):
     A, B = si.integer_copy(70, 90, 110, seed=4)
     C = lib.matmul_host(A, B)
     assert np.array_equal(C.double().numpy(), ref_of(A, B))
+
+
+def persistent_plan(M, N, K, slots):
+    """The persistent kernel's rule for a last, partial wave of 128 x 256 tiles:
+    (first split tile, K slices)."""
+    tiles = -(-M // 128) * -(-N // 256)
+    k_tiles = -(-K // 32)
+    r = tiles % slots
+    if r == 0:
+        return tiles, 1
+    tile_us = 2.0 * 128 * 256 * K / 4.0e5
+    best, S = float(-(-r // slots)), 1
+    for s in range(2, 17):
+        if k_tiles // s < 8:
+            break
+        t = (-(-(r * s) // slots)) / s + ((s - 1) + 2.0) / tile_us
+        if t < best - 1e-9:
+            best, S = t, s
+    if S == 1:
+        return tiles, 1
+    kps = -(-k_tiles // S)
+    return tiles - r, -(-k_tiles // kps)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1664, 3328, 2048),  # 169 whole tiles: the last 17 in K slices
+    (1701, 3341, 2050),  # ragged M, N and K (zero-filled boxes; predicated edge stores)
+    (4096, 4096, 1024),  # 512 tiles: 3 rounds + 56 tiles in slices
+    (520, 1030, 3000),   # fewer tiles than SMs: every tile in slices
+    (256, 256, 4096),    # one tile in 16 slices
+    (100, 8000, 700),    # 32 tiles, K of 22 k-tiles with a ragged last one
+])
+def test_persistent_kernel_one_launch_exact_and_within_tolerance(lib, M, N, K):
+    """The persistent kernel is one launch whatever the split; the slice that finishes a
+    tile last adds every slice's partial in slice order."""
+    import programming_tiled_gemm_gb300 as g
+    slots = torch.cuda.get_device_properties(0).multi_processor_count
+    first, S = persistent_plan(M, N, K, slots)
+    if M >= 1664:
+        assert S > 1  # these shapes exercise the slices
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, 5)
+    Ai, Bi = si.integer_copy(M, N, K, seed=M + N)
+    n0 = lib.launch_count()
+    got = run_padded(lib, Ai, Bi, pad_a=pad_to_16_bytes(K), pad_b=pad_to_16_bytes(N), pad_c=3)
+    assert lib.launch_count() - n0 == 1
+    assert np.array_equal(got, ref_of(Ai, Bi))
+    A, B = si.gemm_operands(M, N, K, seed=M + N + 1)
+    got = run_padded(lib, A, B, pad_a=pad_to_16_bytes(K), pad_b=pad_to_16_bytes(N))
+    assert np.abs(got - ref_of(A, B)).max() <= 1e-5 * math.sqrt(K)
+
+
+def test_persistent_kernel_is_the_default_for_aligned_operands(lib):
+    """With 16-byte rows (M > 64) the default choice is the persistent kernel: one launch."""
+    A, B = si.integer_copy(1024, 1024, 512, seed=41)
+    Ad, Bd = A.cuda(), B.cuda()
+    n0 = lib.launch_count()
+    C = lib.matmul(Ad, Bd)
+    assert lib.launch_count() - n0 == 1
+    assert np.array_equal(C.cpu().double().numpy(), ref_of(A, B))
+
+
+def test_persistent_kernel_refuses_unaligned_rows(lib):
+    import programming_tiled_gemm_gb300 as g
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, 5)
+    A = torch.ones((100, 66), device="cuda")
+    C = torch.empty((100, 66), device="cuda")
+    h = lib.handle
+    # lda = 66: rows of A are not a multiple of 16 bytes
+    assert g.gemm_run(h, 100, 64, 66, A.data_ptr(), 66, A.data_ptr(), 66, C.data_ptr(), 66, 0) == g.GEMM_ERR_ALIGNMENT
+
+
+def test_persistent_forced_split_matches_the_split_partials_of_the_tiled_kernel(lib):
+    """A forced split cuts every tile at the same k-tile boundaries as the tiled kernel's
+    split-K, and both add the slices in slice order: the two agree bit for bit."""
+    import programming_tiled_gemm_gb300 as g
+    A, B = si.gemm_operands(384, 512, 2000, seed=43)
+    Ad, Bd = A.cuda(), B.cuda()
+    lib.set_option(g.GEMM_OPT_SPLIT_K, 5)
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, 5)
+    c5 = lib.matmul(Ad, Bd).clone()
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, 1)
+    c1 = lib.matmul(Ad, Bd)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    assert np.abs(c5.cpu().double().numpy() - ref_of(A, B)).max() <= 1e-5 * math.sqrt(2000)
+    assert np.abs(c5.cpu().double().numpy() - c1.cpu().double().numpy()).max() <= 2e-5 * math.sqrt(2000)

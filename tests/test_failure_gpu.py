@@ -1,6 +1,6 @@
 """Failure detection on the GPU without a fault.
 
-Every mbarrier wait in the tensor-core kernels and the TMA-fed skinny kernel is bounded
+Every mbarrier wait in the tensor-core kernels and the TMA-fed fp32 kernels is bounded
 by a wall-clock limit.  GEMM_OPT_TEST_STALL makes the kernel wait once on a barrier that
 nothing ever arrives on, so that wait runs out: the kernel records a timeout in the
 handle's status word, lets its other roles give up, waits (bounded) for the copies and
@@ -64,6 +64,23 @@ def test_skinny_wait_runs_out_and_is_reported(lib):
     torch.cuda.synchronize()
     assert lib.device_status() == g.GEMM_OK
     assert np.array_equal(C.cpu().double().numpy(), oracle.gemm(A.numpy(), B.numpy()))
+
+
+def test_persistent_fp32_wait_runs_out_and_is_reported(lib):
+    import programming_tiled_gemm_gb300 as g
+    dev = torch.device("cuda")
+    A, B = si.integer_copy(700, 900, 1000, seed=33)
+    Ad, Bd = A.to(dev), B.to(dev)
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, 5)
+    lib.set_option(g.GEMM_OPT_TEST_STALL, 1)
+    lib.matmul(Ad, Bd)
+    assert lib.device_status() == g.GEMM_ERR_DEVICE_TIMEOUT
+    lib.set_option(g.GEMM_OPT_TEST_STALL, 0)
+    C = lib.matmul(Ad, Bd)
+    torch.cuda.synchronize()
+    assert lib.device_status() == g.GEMM_OK
+    assert np.array_equal(C.cpu().double().numpy(), oracle.gemm(A.numpy(), B.numpy()))
+    lib.set_option(g.GEMM_OPT_F32_KERNEL, 0)
 
 
 def test_test_hook_rejects_other_values(lib):
