@@ -59,7 +59,9 @@ typedef enum {
     GEMM_ERR_ALIGNMENT = -2,      /* bf16/fp16: base not 16-byte aligned or ld*2 % 16 != 0 */
     GEMM_ERR_UNSUPPORTED = -3,    /* device is not sm_103, or a size beyond a kernel limit */
     GEMM_ERR_CUDA = -4,           /* a CUDA runtime call or a launch failed */
-    GEMM_ERR_DEVICE_TIMEOUT = -5  /* a kernel's bounded wait ran out (see gemm_get_device_status) */
+    GEMM_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait ran out (see gemm_get_device_status) */
+    GEMM_ERR_DEVICE_BOUNDS = -6   /* debug library only: a kernel's index check failed and the access was
+                                     skipped (see gemm_get_device_status) */
 } gemm_status_t;
 
 /* Create a handle bound to CUDA device `device`.  Queries the SM count, allocates the
@@ -215,13 +217,21 @@ int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t 
 int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
                       int64_t C_out, const int64_t k_dims[4], float* y, int dtype, void* stream);
 
-/* Synchronise `stream`, then read and clear the handle's device status word.  This is
+/* Synchronise `stream`, then read and clear the handle's device status word (and, in the
+ * debug library, the kernels' bounds-check flags).  This is
  * the wait of "Learning to develop for GPU with GEMM as the example", section "Writing a
  * GPU implementation of matrix multiplication" (its part on launching the kernel: the host
  * waits on an event for the enqueued kernel), extended with the kernel's own report.
  * Returns GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a kernel launched through this
  * handle gave up on a bounded wait since the last call (its output is then invalid),
- * or GEMM_ERR_CUDA if the stream reports an error. */
+ * GEMM_ERR_DEVICE_BOUNDS (debug library, lib/libgemm_gb300_debug.so, built with
+ * -DGEMM_DEBUG) if a kernel of this process found a computed global index outside its
+ * operand since the last call and skipped that access (the output is then invalid; these
+ * flags are per process and device, not per handle), or GEMM_ERR_CUDA if the stream
+ * reports an error.
+ * Debugging aids: the environment variable GEMM_LOG=1 makes the library print, on stderr,
+ * one line per call with the kernel it chose, its split of K and the workspace it uses,
+ * and the reason for every refused call; any other value (or none) prints nothing. */
 int gemm_get_device_status(gemm_handle_t h, void* stream);
 
 /* Tuning and test options (see GEMM_OPT_*).  Values outside the documented range are

@@ -11,7 +11,10 @@ import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "lib", "libgemm_gb300.so")
+# GEMM_GB300_DEBUG=1 loads the debug build (every computed global index checked in the
+# kernels; a failed check is reported by gemm_get_device_status as GEMM_ERR_DEVICE_BOUNDS).
+DEBUG = os.environ.get("GEMM_GB300_DEBUG") == "1"
+LIB_PATH = os.path.join(_PKG, "lib", "libgemm_gb300_debug.so" if DEBUG else "libgemm_gb300.so")
 
 GEMM_F32, GEMM_BF16, GEMM_F16 = 0, 1, 2
 GEMM_OK = 0
@@ -20,6 +23,7 @@ GEMM_ERR_ALIGNMENT = -2
 GEMM_ERR_UNSUPPORTED = -3
 GEMM_ERR_CUDA = -4
 GEMM_ERR_DEVICE_TIMEOUT = -5
+GEMM_ERR_DEVICE_BOUNDS = -6
 GEMM_OPT_F32_KERNEL, GEMM_OPT_SPLIT_K, GEMM_OPT_WAIT_LIMIT_US, GEMM_OPT_TC_CHUNK, GEMM_OPT_TC_PAIR = 1, 2, 3, 4, 5
 GEMM_OPT_TEST_STALL = 6
 GEMM_OPT_CONV_STACK = 7
@@ -47,7 +51,7 @@ class GemmError(RuntimeError):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError("libgemm_gb300.so is not built (%s); run __graft_entry__.build() first" % LIB_PATH)
+        raise ImportError("%s is not built; run __graft_entry__.build() first" % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
     i64, p, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
     lib.gemm_create.argtypes = [ctypes.POINTER(p), i32]

@@ -1,7 +1,10 @@
 """Build the CUDA library in-tree: one nvcc process per translation unit, then a link.
 
-Output: ``programming_tiled_gemm_gb300/lib/libgemm_gb300.so`` (sm_103a only).
-Object files go to ``programming_tiled_gemm_gb300/_build/``.  Nothing is installed.
+Output: ``programming_tiled_gemm_gb300/lib/libgemm_gb300.so`` (sm_103a only), and with
+``debug=True`` ``lib/libgemm_gb300_debug.so``: the same sources built with -DGEMM_DEBUG,
+whose kernels check every computed global index before the access (see internal.h).
+Object files go to ``programming_tiled_gemm_gb300/_build/`` (``_build/debug/``).  Nothing is
+installed.
 """
 from __future__ import annotations
 
@@ -17,6 +20,7 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libgemm_gb300.so")
+LIB_DEBUG = os.path.join(LIBDIR, "libgemm_gb300_debug.so")
 
 SOURCES = ["api.cu", "ffma.cu", "ffma_tma.cu", "skinny.cu", "skinny_tma.cu", "im2col.cu", "conv_implicit.cu", "conv_tc.cu", "tc_gemm.cu",
            "skinny_noalloc.cu"]
@@ -49,8 +53,11 @@ def _stale(obj: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, ptxas_verbose: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_verbose: bool = False, force: bool = False, debug: bool = False) -> str:
+    objdir = os.path.join(BUILD, "debug") if debug else BUILD
+    lib_path = LIB_DEBUG if debug else LIB
+    defines = ["-DGEMM_DEBUG"] if debug else []
+    os.makedirs(objdir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "gemm.h"))
@@ -58,10 +65,10 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, force: bool = Fals
     objs = []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
         objs.append(obj)
         if force or _stale(obj, [path] + headers):
-            cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", path, "-o", obj]
+            cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *defines, "-I", INCLUDE, "-c", path, "-o", obj]
             if ptxas_verbose:
                 cmd += ["-Xptxas", "-v"]
             jobs.append(cmd)
@@ -79,18 +86,17 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, force: bool = Fals
                 failed.append(cmd[-3])
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp.%d" % os.getpid()
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + ".tmp.%d" % os.getpid()
         libdir = cuda_lib_dir()
         cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", "-rpath," + libdir, "-L" + libdir]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:
             raise RuntimeError("link failed:\n" + p.stdout + p.stderr)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(verbose=True, ptxas_verbose="-v" in sys.argv, force="-f" in sys.argv)
-    print(LIB)
+    print(build(verbose=True, ptxas_verbose="-v" in sys.argv, force="-f" in sys.argv, debug="--debug" in sys.argv))

@@ -12,11 +12,38 @@
 #include <new>
 #include <vector>
 
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
 #include "internal.h"
 
 using namespace gemm_gb300;
 
 namespace gemm_gb300 {
+
+bool log_enabled()
+{
+    static const bool on = [] {
+        const char* v = getenv("GEMM_LOG");
+        return v && strcmp(v, "1") == 0;
+    }();
+    return on;
+}
+
+void glog(const char* fmt, ...)
+{
+    if (!log_enabled()) return;
+    va_list ap;
+    va_start(ap, fmt);
+    char line[512];
+    vsnprintf(line, sizeof(line), fmt, ap);
+    va_end(ap);
+    fprintf(stderr, "[gemm] %s\n", line);
+}
+
+const char* dtype_name(int d) { return d == GEMM_F32 ? "f32" : d == GEMM_BF16 ? "bf16" : d == GEMM_F16 ? "f16" : "?"; }
 
 int check_product_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                        const void* C, int64_t ldc)
@@ -160,6 +187,9 @@ int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)
         int rc = tagged_counters(&h->f32_counters, &h->f32_counters_bytes, &h->f32_seq, pl.counters, stream);
         if (rc != GEMM_OK) return rc;
         const uint32_t seq = h->f32_seq;
+        glog("f32 %lldx%lldx%lld: persistent FFMA kernel (5), %lld tiles of 128x256, tiles from %lld in %d K slices, "
+             "workspace %lld bytes", (long long)a.M, (long long)a.N, (long long)a.K, (long long)pl.tiles,
+             (long long)pl.split_first, pl.split, (long long)(pl.ws_floats * 4));
         int n = 0;
         cudaError_t e = launch_ffma_persistent(a, pl, h->workspace, h->f32_counters, seq, h->num_sms, h->d_status,
                                                h->wait_limit_ns, h->opt_test_stall, stream, &n);
@@ -181,6 +211,11 @@ int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)
         int rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, need);
         if (rc != GEMM_OK) return rc;
     }
+    glog("f32 %lldx%lldx%lld: kernel %d (%s), split %d, workspace %zu bytes", (long long)a.M, (long long)a.N,
+         (long long)a.K, kernel,
+         kernel == 1 ? "tiled 128x256 FFMA" : kernel == 2 ? "tiled 64x128 FFMA" : kernel == 3 ? "skinny, registers"
+                                                                                             : "skinny, TMA ring",
+         split, need);
     cudaError_t e;
     int n = 0;
     if (kernel == 4)
@@ -198,7 +233,7 @@ int run_f32(gemm_handle_t h, const F32Args& a, cudaStream_t stream)
 
 extern "C" {
 
-int gemm_create(gemm_handle_t* out, int device)
+static int gemm_create_impl(gemm_handle_t* out, int device)
 {
     if (!out) return GEMM_ERR_INVALID_ARG;
     *out = nullptr;
@@ -250,7 +285,7 @@ int gemm_destroy(gemm_handle_t h)
     return GEMM_OK;
 }
 
-int gemm_set_option(gemm_handle_t h, int option, int64_t value)
+static int gemm_set_option_impl(gemm_handle_t h, int option, int64_t value)
 {
     if (!h) return GEMM_ERR_INVALID_ARG;
     switch (option) {
@@ -287,7 +322,7 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     }
 }
 
-int gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+static int gemm_run_ex_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                 const void* B, int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t ab_dtype,
                 gemm_dtype_t c_dtype, void* stream)
 {
@@ -355,6 +390,10 @@ int gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha, c
         t.rem_flag = reinterpret_cast<uint32_t*>(h->tc_counters + need.counters);
         t.rem_seq = h->tc_seq;
     }
+    glog("%s %lldx%lldx%lld: tensor-core GEMM (tile option %d: 0 choose, 1 single CTA, 2 CTA pair), last-wave "
+         "K-split workspace %lld floats and %lld counters, chunk %d k-blocks",
+         dtype_name(ab_dtype), (long long)M, (long long)N, (long long)K, h->opt_tc_pair, (long long)need.floats,
+         (long long)need.counters, h->opt_tc_chunk > 0 ? h->opt_tc_chunk : 16);
     int n = 0;
     int rc2 = launch_tc_gemm(t, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_tc_chunk, h->opt_tc_pair, s, &n);
     h->launches += n;
@@ -585,7 +624,7 @@ extern "C" int gemm_run_host_batch(gemm_handle_t h, int count, const gemm_host_p
 
 extern "C" {
 
-int conv4d_im2col(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4],
+static int conv4d_im2col_impl(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4],
                   const int64_t k_dims[4], float* col, void* stream)
 {
     if (!h || !x || !col || !in_dims || !k_dims || C_in <= 0) return GEMM_ERR_INVALID_ARG;
@@ -605,7 +644,7 @@ int64_t gemm_launch_count(gemm_handle_t h)
     return h ? h->launches : -1;
 }
 
-int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4], const float* w,
+static int conv4d_forward_impl(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4], const float* w,
                    int64_t C_out, const int64_t k_dims[4], float* y, int64_t ldy, void* stream)
 {
     if (!h || !x || !w || !y || !in_dims || !k_dims || C_in <= 0 || C_out <= 0) return GEMM_ERR_INVALID_ARG;
@@ -631,6 +670,8 @@ int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t 
         int rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, need);
         if (rc != GEMM_OK) return rc;
     }
+    glog("conv4d_forward: implicit GEMM, %lld output positions, %d tap groups, split %d, workspace %lld bytes",
+         (long long)npos, ngroups, split, split > 1 ? (long long)split * cblock * npos * 4 : 0ll);
     // output channels in blocks of 32 (rows of W and y)
     for (int64_t o0 = 0; o0 < C_out; o0 += 32) {
         const int64_t nc = (C_out - o0) < 32 ? (C_out - o0) : 32;
@@ -643,7 +684,7 @@ int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t 
     return GEMM_OK;
 }
 
-int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
+static int conv4d_forward_cl_impl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
                       int64_t C_out, const int64_t k_dims[4], float* y, int dtype, void* stream)
 {
     if (!h || !x || !w || !y || !in_dims || !k_dims || C_in <= 0 || C_out <= 0) return GEMM_ERR_INVALID_ARG;
@@ -660,6 +701,8 @@ int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_
     if (ws < 0) return GEMM_ERR_UNSUPPORTED;
     int rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, (size_t)ws);
     if (rc != GEMM_OK) return rc;
+    glog("conv4d_forward_cl: tensor-core convolution, staged operands %lld bytes (stack option %d)", (long long)ws,
+         h->opt_conv_stack);
     int n = 0;
     rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, dtype == GEMM_BF16, h->opt_conv_stack, h->workspace,
                           h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall,
@@ -678,8 +721,23 @@ int gemm_get_device_status(gemm_handle_t h, void* stream)
     if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
     if (v != 0) {
         if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+        glog("gemm_get_device_status: a bounded wait ran out (device code %d)", v);
         return GEMM_ERR_DEVICE_TIMEOUT;
     }
+#ifdef GEMM_DEBUG
+    int bad = 0;
+    for (auto take : {bounds_flag_take_ffma, bounds_flag_take_ffma_tma, bounds_flag_take_skinny,
+                      bounds_flag_take_skinny_tma, bounds_flag_take_im2col, bounds_flag_take_conv_implicit,
+                      bounds_flag_take_conv_tc, bounds_flag_take_tc_gemm}) {
+        const int r = take();
+        if (r < 0) return GEMM_ERR_CUDA;
+        bad |= r;
+    }
+    if (bad) {
+        glog("gemm_get_device_status: a kernel's index check failed (debug build)");
+        return GEMM_ERR_DEVICE_BOUNDS;
+    }
+#endif
     return GEMM_OK;
 }
 
@@ -692,8 +750,71 @@ const char* gemm_status_string(int status)
     case GEMM_ERR_UNSUPPORTED: return "unsupported device or size";
     case GEMM_ERR_CUDA: return "CUDA runtime error";
     case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait; its output is invalid";
+    case GEMM_ERR_DEVICE_BOUNDS: return "a kernel's index check failed and the access was skipped (debug build); its output is invalid";
     default: return "unknown status";
     }
+}
+
+}  // extern "C"
+
+// Entry points: each forwards to its implementation above and, with GEMM_LOG=1, reports a
+// refused call with its arguments.
+extern "C" {
+
+int gemm_create(gemm_handle_t* out, int device)
+{
+    const int rc = gemm_create_impl(out, device);
+    if (rc != GEMM_OK) glog("gemm_create(device %d) refused: %s (%d)", device, gemm_status_string(rc), rc);
+    else glog("gemm_create(device %d): %d SMs", device, (*out)->num_sms);
+    return rc;
+}
+
+int gemm_set_option(gemm_handle_t h, int option, int64_t value)
+{
+    const int rc = gemm_set_option_impl(h, option, value);
+    if (rc != GEMM_OK)
+        glog("gemm_set_option(%d, %lld) refused: %s (%d)", option, (long long)value, gemm_status_string(rc), rc);
+    return rc;
+}
+
+int gemm_run_ex(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                const void* B, int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t ab_dtype,
+                gemm_dtype_t c_dtype, void* stream)
+{
+    const int rc = gemm_run_ex_impl(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ab_dtype, c_dtype, stream);
+    if (rc != GEMM_OK)
+        glog("gemm_run(%s, M %lld, N %lld, K %lld, lda %lld, ldb %lld, ldc %lld, A %p, B %p, C %p) refused: %s (%d)",
+             dtype_name(ab_dtype), (long long)M, (long long)N, (long long)K, (long long)lda, (long long)ldb,
+             (long long)ldc, A, B, C, gemm_status_string(rc), rc);
+    return rc;
+}
+
+int conv4d_im2col(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4], const int64_t k_dims[4],
+                  float* col, void* stream)
+{
+    const int rc = conv4d_im2col_impl(h, x, C_in, in_dims, k_dims, col, stream);
+    if (rc != GEMM_OK) glog("conv4d_im2col(C_in %lld) refused: %s (%d)", (long long)C_in, gemm_status_string(rc), rc);
+    return rc;
+}
+
+int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t in_dims[4], const float* w,
+                   int64_t C_out, const int64_t k_dims[4], float* y, int64_t ldy, void* stream)
+{
+    const int rc = conv4d_forward_impl(h, x, C_in, in_dims, w, C_out, k_dims, y, ldy, stream);
+    if (rc != GEMM_OK)
+        glog("conv4d_forward(C_in %lld, C_out %lld, ldy %lld) refused: %s (%d)", (long long)C_in, (long long)C_out,
+             (long long)ldy, gemm_status_string(rc), rc);
+    return rc;
+}
+
+int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
+                      int64_t C_out, const int64_t k_dims[4], float* y, int dtype, void* stream)
+{
+    const int rc = conv4d_forward_cl_impl(h, x, C_in, in_dims, w, C_out, k_dims, y, dtype, stream);
+    if (rc != GEMM_OK)
+        glog("conv4d_forward_cl(C_in %lld, C_out %lld, %s) refused: %s (%d)", (long long)C_in, (long long)C_out,
+             dtype_name(dtype), gemm_status_string(rc), rc);
+    return rc;
 }
 
 }  // extern "C"

@@ -24,6 +24,9 @@
 #include "internal.h"
 
 namespace gemm_gb300 {
+
+GEMM_DEBUG_UNIT(conv_implicit)
+
 namespace {
 
 constexpr int CI_COL_THREADS = 256;                 // threads across positions (4 each)
@@ -135,7 +138,8 @@ __global__ void __launch_bounds__(CI_THREADS, 1) conv4d_implicit_kernel(ConvPara
                 if (e < ntap_chunk * CI_MR) {
                     const int tap = e / CI_MR, m = e % CI_MR;
                     const int q = qc + tap / g.r3;
-                    if (m < g.cout && q < q_end) v = __ldg(p.w + (int64_t)m * g.ntaps + (int64_t)q * g.r3 + tap % g.r3);
+                    if (m < g.cout && q < q_end && in_range(m, g.cout) && in_range((int64_t)q * g.r3 + tap % g.r3, g.ntaps))
+                        v = __ldg(p.w + (int64_t)m * g.ntaps + (int64_t)q * g.r3 + tap % g.r3);
                 }
                 wreg[i] = v;
             }
@@ -153,7 +157,8 @@ __global__ void __launch_bounds__(CI_THREADS, 1) conv4d_implicit_kernel(ConvPara
         // x values of one tap group: 8 floats starting at the thread's first position
         auto load_x = [&](int64_t gb, float (&v)[8]) {
             if constexpr (VEC) {
-                if (pos_ok) {
+                if (pos_ok && in_range(gb + pbase[0], (int64_t)g.cin * g.chan_stride) &&
+                    in_range(gb + pbase[0] + 7, (int64_t)g.cin * g.chan_stride)) {
                     const float4* src = reinterpret_cast<const float4*>(p.x + gb + pbase[0]);
                     const float4 lo = __ldg(src);
                     const float4 hi = __ldg(src + 1);
@@ -204,7 +209,9 @@ __global__ void __launch_bounds__(CI_THREADS, 1) conv4d_implicit_kernel(ConvPara
                         float2 sd[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const float s1 = (n0 + j < g.npos) ? __ldg(p.x + gb + pbase[j] + r3) : 0.f;
+                            const float s1 = (n0 + j < g.npos && in_range(gb + pbase[j] + r3, (int64_t)g.cin * g.chan_stride))
+                                                 ? __ldg(p.x + gb + pbase[j] + r3)
+                                                 : 0.f;
                             sd[j] = make_float2(s1, s1);
                         }
                         const float* wrow = &wsm[buf][qi * g.r3 + r3][m_base];
@@ -239,12 +246,13 @@ __global__ void __launch_bounds__(CI_THREADS, 1) conv4d_implicit_kernel(ConvPara
 #pragma unroll
             for (int m = 0; m < CI_RT; ++m) {
                 if (m_base + m >= g.cout) break;
+                if (!in_range(m_base + m, g.cout) || !in_range(n0, g.npos)) break;
                 float* dst = out + (int64_t)(m_base + m) * ldo + n0;
                 float o[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) o[j] = (m % 2 == 0) ? acc[m / 2][j].x : acc[m / 2][j].y;
                 if (p.vec_out && n0 + 3 < g.npos) {
-                    *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+                    if (in_range(n0 + 3, g.npos)) *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)

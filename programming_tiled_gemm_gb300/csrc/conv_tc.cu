@@ -46,6 +46,9 @@
 #include "ptx.h"
 
 namespace gemm_gb300 {
+
+GEMM_DEBUG_UNIT(conv_tc)
+
 namespace {
 
 constexpr int CT_MAX_ISSUERS = 8;   // warps whose lane 0 issues MMAs (fewer when TMEM holds fewer accumulators)
@@ -80,6 +83,7 @@ struct ConvTcParams {
     uint32_t idesc;
     const uint8_t* xp;  // staged input (workspace)
     const uint8_t* wp;  // staged weights (workspace)
+    int64_t xp_bytes, wp_bytes;  // their sizes (index checks of debug builds)
     float* y;
     int* status;
     uint64_t limit_ns;
@@ -128,26 +132,30 @@ conv_tc_prepare_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w,
             const int i3 = pos % p.I[3], rest = pos / p.I[3];
             const int row = rest % plane_rows, i0 = rest / plane_rows;
             const int ph = i3 % S, m = i3 / S;
-            xp[((int64_t)((i0 * cg + g) * S + ph) * p.xp_rows + row) * mS + m] = x[e];
+            const int64_t d = ((int64_t)((i0 * cg + g) * S + ph) * p.xp_rows + row) * mS + m;
+            if (in_range(d, p.xp_bytes / 16)) xp[d] = x[e];
         } else if (e < n_x + n_xz) {
             const int f = e - n_x;
             const int m = f % mS, r = f / mS;
             const int row = plane_rows + r % tail, blk = r / tail;  // blk = (i0 * cg + g) * S + ph
-            xp[((int64_t)blk * p.xp_rows + row) * mS + m] = zero;
+            const int64_t d = ((int64_t)blk * p.xp_rows + row) * mS + m;
+            if (in_range(d, p.xp_bytes / 16)) xp[d] = zero;
         } else if (e < n_x + n_xz + n_w) {
             const int f = e - n_x - n_xz;
             const int g = f % cg, r = f / cg;
             const int r3 = r % p.R[3], r2 = r / p.R[3];
             const int trip = r2 % trips, o = r2 / trips;
             const int j = p.R[3] + S - 2 - r3;
-            wp[((int64_t)(trip * cg + g) * p.nslices + j) * p.cout + o] = w[f];
+            const int64_t d = ((int64_t)(trip * cg + g) * p.nslices + j) * p.cout + o;
+            if (in_range(d, p.wp_bytes / 16)) wp[d] = w[f];
         } else {
             const int f = e - n_x - n_xz - n_w;
             const int o = f % p.cout, r = f / p.cout;
             const int z = r % zs, r2 = r / zs;  // z < S - 1: the first slices, else the last
             const int g = r2 % cg, trip = r2 / cg;
             const int j = z < S - 1 ? z : p.R[3] + S - 1 + (z - (S - 1));
-            wp[((int64_t)(trip * cg + g) * p.nslices + j) * p.cout + o] = zero;
+            const int64_t d = ((int64_t)(trip * cg + g) * p.nslices + j) * p.cout + o;
+            if (in_range(d, p.wp_bytes / 16)) wp[d] = zero;
         }
     }
 }
@@ -221,11 +229,17 @@ __global__ void __launch_bounds__(CT_THREADS, 1) conv4d_tc_kernel(ConvTcParams p
                 const uint32_t fb = smem_u32(&full_bar[slot]);
                 mbar_arrive_expect_tx(fb, (uint32_t)(cgroups * p.S) * a_bytes + (uint32_t)(g * p.b_trip));
                 uint8_t* a_dst = smem + slot * p.stage_bytes;
-                const uint8_t* src = p.xp + ((int64_t)(p0 + r0) * cgroups * p.S) * blk_stride + row * row_bytes;
+                const int64_t src_off = ((int64_t)(p0 + r0) * cgroups * p.S) * blk_stride + row * row_bytes;
+                const uint8_t* src = p.xp + src_off;
+                // (debug builds: a copy outside the staged operands is skipped; its stage then
+                // never completes and the consumers' bounded wait reports it)
                 for (int b = 0; b < cgroups * p.S; ++b)
-                    bulk_load(smem_u32(a_dst + b * p.a_blk), src + b * blk_stride, a_bytes, fb);
+                    if (in_range(src_off + b * blk_stride, p.xp_bytes) &&
+                        in_range(src_off + b * blk_stride + a_bytes - 1, p.xp_bytes))
+                        bulk_load(smem_u32(a_dst + b * p.a_blk), src + b * blk_stride, a_bytes, fb);
                 const int64_t trip = ((int64_t)r0 * p.R[1] + r1) * p.R[2] + r2s;
-                bulk_load(smem_u32(a_dst + p.a_region), p.wp + trip * p.b_trip, (uint32_t)(g * p.b_trip), fb);
+                if (in_range(trip * p.b_trip, p.wp_bytes) && in_range(trip * p.b_trip + g * p.b_trip - 1, p.wp_bytes))
+                    bulk_load(smem_u32(a_dst + p.a_region), p.wp + trip * p.b_trip, (uint32_t)(g * p.b_trip), fb);
                 issued_mask |= 1u << slot;
                 last_parity = (last_parity & ~(1u << slot)) | (ph << slot);
                 if (++slot == SA) {
@@ -361,7 +375,7 @@ __global__ void __launch_bounds__(CT_THREADS, 1) conv4d_tc_kernel(ConvTcParams p
                 const int u = u0 + g * p.S + t;
                 const int p1 = u / plane, rem = u - p1 * plane;
                 const int p2 = rem / p.I[3], p3 = rem - p2 * p.I[3];
-                if (p1 < p.P[1] && p2 < p.P[2] && p3 < p.P[3]) {
+                if (p1 < p.P[1] && p2 < p.P[2] && p3 < p.P[3] && in_range(p0, p.P[0]) && in_range(o0 + 15, p.cout)) {
                     float* yrow = p.y + ((((int64_t)p0 * p.P[1] + p1) * p.P[2] + p2) * p.P[3] + p3) * p.cout + o0;
 #pragma unroll
                     for (int i = 0; i < 16; i += 4)
@@ -514,6 +528,8 @@ int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.xp = ws;
     p.wp = ws + xb;
+    p.xp_bytes = xb;
+    p.wp_bytes = (int64_t)p.R[0] * p.R[1] * p.R[2] * p.b_trip;
     p.idesc = conv_idesc(bf16, S * p.cout);
     p.y = y;
     p.status = dev_status;

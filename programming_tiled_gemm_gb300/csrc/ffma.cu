@@ -24,6 +24,9 @@
 #include "internal.h"
 
 namespace gemm_gb300 {
+
+GEMM_DEBUG_UNIT(ffma)
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -94,10 +97,10 @@ ffma_tiled_kernel(const float* __restrict__ A, int lda, const float* __restrict_
                 const int row = f / (BK / 4);
                 const int kq = (f % (BK / 4)) * 4;
                 const int64_t gm = m0 + row, gk = k0 + kq;
-                if (gm < p.M) {
+                if (gm < p.M && in_range(gm, p.M)) {
                     const float* src = p.A + gm * p.lda + gk;
                     if (VEC && gk + 3 < kend) {
-                        v = __ldg(reinterpret_cast<const float4*>(src));
+                        if (in_range(gk + 3, p.K)) v = __ldg(reinterpret_cast<const float4*>(src));
                     } else {
                         if (gk + 0 < kend) v.x = __ldg(src + 0);
                         if (gk + 1 < kend) v.y = __ldg(src + 1);
@@ -116,10 +119,10 @@ ffma_tiled_kernel(const float* __restrict__ A, int lda, const float* __restrict_
                 const int krow = f / (BN / 4);
                 const int nq = (f % (BN / 4)) * 4;
                 const int64_t gk = k0 + krow, gn = n0 + nq;
-                if (gk < kend) {
+                if (gk < kend && in_range(gk, p.K)) {
                     const float* src = p.B + gk * p.ldb + gn;
                     if (VEC && gn + 3 < p.N) {
-                        v = __ldg(reinterpret_cast<const float4*>(src));
+                        if (in_range(gn + 3, p.N)) v = __ldg(reinterpret_cast<const float4*>(src));
                     } else {
                         if (gn + 0 < p.N) v.x = __ldg(src + 0);
                         if (gn + 1 < p.N) v.y = __ldg(src + 1);
@@ -207,14 +210,14 @@ ffma_tiled_kernel(const float* __restrict__ A, int lda, const float* __restrict_
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int64_t gm = m0 + ty * 4 + a * TY * 4 + i;
-            if (gm >= p.M) continue;
+            if (gm >= p.M || !in_range(gm, p.M)) continue;
             float* row = out + gm * ldo;
 #pragma unroll
             for (int b = 0; b < TN / 4; ++b) {
                 const int64_t gn = n0 + tx * 4 + b * TX * 4;
                 const float* v = &acc[a * 4 + i][b * 4];
                 if (vec_out && gn + 3 < p.N) {
-                    *reinterpret_cast<float4*>(row + gn) = make_float4(v[0], v[1], v[2], v[3]);
+                    if (in_range(gn + 3, p.N)) *reinterpret_cast<float4*>(row + gn) = make_float4(v[0], v[1], v[2], v[3]);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
@@ -335,10 +338,15 @@ ffma_warptile_kernel(const float* __restrict__ A, int lda_, const float* __restr
     int k_next = kbeg;  // k of the tile the next load() fetches
     auto load = [&]() {
         if constexpr (!EDGE) {
-            ra[0] = __ldg(reinterpret_cast<const float4*>(a_cur));
-            ra[1] = __ldg(reinterpret_cast<const float4*>(a_cur + 8));
+            // (the index checks compile away outside debug builds)
+            if (in_range(m0 + a_row, M) && in_range(k_next + a_kq + 11, K)) {
+                ra[0] = __ldg(reinterpret_cast<const float4*>(a_cur));
+                ra[1] = __ldg(reinterpret_cast<const float4*>(a_cur + 8));
+            }
+            if (in_range(k_next + b_k + 12, K) && in_range(n0 + b_nq + 3, N))
 #pragma unroll
-            for (int h = 0; h < 4; ++h) rb[h] = __ldg(reinterpret_cast<const float4*>(b_cur + h * b_step));
+                for (int h = 0; h < 4; ++h) rb[h] = __ldg(reinterpret_cast<const float4*>(b_cur + h * b_step));
+            k_next += W_BK;
         } else {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -461,13 +469,14 @@ ffma_warptile_kernel(const float* __restrict__ A, int lda_, const float* __restr
     for (int i = 0; i < 8; ++i) {
         const int64_t gm = m0 + a_frag + (i / 4) * 32 + (i % 4);
         if (EDGE && gm >= M) continue;
+        if (!in_range(gm, M)) continue;
         float* row = out + (gm - row0) * ldo - col0;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             const int64_t gn = n0 + b_frag + h * 16;
             const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y};
             if ((vec_out || tmap.compact) && (!EDGE || gn + 3 < N)) {
-                *reinterpret_cast<float4*>(row + gn) = make_float4(v[0], v[1], v[2], v[3]);
+                if (in_range(gn + 3, N)) *reinterpret_cast<float4*>(row + gn) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
@@ -481,7 +490,7 @@ ffma_warptile_kernel(const float* __restrict__ A, int lda_, const float* __restr
 // C[tile element] = part 0 + part 1 + ... for the tiles first .. first + ntiles - 1.
 __global__ void __launch_bounds__(256)
 splitk_reduce_tiles_kernel(const float* __restrict__ ws, int split, TileMap tmap, int ntiles, float* __restrict__ C,
-                           int64_t ldc)
+                           int64_t ldc, int M, int N)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the partials' writer has finished
     constexpr int TILE = W_BM * W_BN;
@@ -498,7 +507,9 @@ splitk_reduce_tiles_kernel(const float* __restrict__ ws, int split, TileMap tmap
         }
         int mt, nt;
         map_tile(tmap, tmap.first + t, mt, nt);
-        float* dst = C + ((int64_t)mt * W_BM + w / W_BN) * ldc + (int64_t)nt * W_BN + w % W_BN;
+        const int64_t r = (int64_t)mt * W_BM + w / W_BN, c = (int64_t)nt * W_BN + w % W_BN;
+        if (!in_range(r, M) || !in_range(c + 3, N)) continue;
+        float* dst = C + r * ldc + c;
         dst[0] = s.x, dst[1] = s.y, dst[2] = s.z, dst[3] = s.w;
     }
 }
@@ -513,6 +524,7 @@ splitk_reduce_kernel(const float* __restrict__ ws, int split, int64_t M, int64_t
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
         const int64_t m = idx / N, n = idx - m * N;
+        if (!in_range(m, M) || !in_range(n, N)) continue;
         float s = ws[idx];
         for (int z = 1; z < split; ++z) s += ws[(int64_t)z * total + idx];
         C[m * ldc + n] = s;
@@ -530,6 +542,7 @@ epilogue_kernel(const float* __restrict__ P, int64_t ldp, void* C, int64_t ldc, 
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
         const int64_t m = idx / N, n = idx - m * N;
+        if (!in_range(m, M) || !in_range(n, N)) continue;
         float v = P ? alpha * P[m * ldp + n] : 0.f;  // no P: an empty product (K == 0)
         const int64_t c = m * ldc + n;
         if (CT == GEMM_F32) {
@@ -639,7 +652,7 @@ cudaError_t launch_warptile(const F32Args& a, int split, float* ws, int remainde
             int64_t blocks = (int64_t)rem * W_BM * W_BN / 4 / 256;
             if (blocks < 1) blocks = 1;
             e = launch_dependent(splitk_reduce_tiles_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, ws, rsplit,
-                                 tr, rem, a.C, a.ldc);
+                                 tr, rem, a.C, a.ldc, (int)a.M, (int)a.N);
             if (e != cudaSuccess) return e;
             *launches += 2;
         }

@@ -36,6 +36,9 @@
 #include "ptx.h"
 
 namespace gemm_gb300 {
+
+GEMM_DEBUG_UNIT(ffma_tma)
+
 namespace {
 
 constexpr int PT_THREADS = 256;
@@ -313,18 +316,20 @@ ffma_persistent_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             // a K slice: publish the partial tile, count it; the last slice to finish adds all
             // slices in slice order and stores C
             const int st = w.tile - p.split_first;
-            float4* base = reinterpret_cast<float4*>(p.ws + (int64_t)st * p.split * PT_TILE_FLOATS);
+            const bool ws_ok = in_range(st, p.num_tiles - p.split_first) && in_range(w.sl, p.split);
+            float4* base = reinterpret_cast<float4*>(p.ws + (int64_t)(ws_ok ? st : 0) * p.split * PT_TILE_FLOATS);
             float4* mine = base + (int64_t)w.sl * (PT_TILE_FLOATS / 4) + tid;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int h = 0; h < 4; ++h)
-                    __stcg(mine + (i * 4 + h) * PT_THREADS,
-                           make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y));
+                    if (ws_ok)
+                        __stcg(mine + (i * 4 + h) * PT_THREADS,
+                               make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y));
             __threadfence();
             __syncthreads();
             if (tid == 0) {
-                const int n = pt_slice_arrive(p.cnt + st, p.seq);
+                const int n = ws_ok ? pt_slice_arrive(p.cnt + st, p.seq) : 0;
                 if (n == 0) pt_fail(p.status, kDevTimeoutEpilogue, abort_flag);
                 *bcast = n;
             }
@@ -364,17 +369,19 @@ ffma_persistent_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         for (int i = 0; i < 8; ++i) {
             const int gm = row0 + 8 * i;
             if (!whole && gm >= p.M) continue;
+            if (!in_range(gm, p.M)) continue;
             float* crow = p.C + (int64_t)gm * p.ldc;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 const int gn = col0 + 16 * h;
                 const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y};
                 if (whole || (p.vec_out && gn + 3 < p.N)) {
-                    st_global_v4_hint(crow + gn, v[0], v[1], v[2], v[3], pol_out);
+                    if (in_range(gn, p.N) && in_range(gn + 3, p.N))
+                        st_global_v4_hint(crow + gn, v[0], v[1], v[2], v[3], pol_out);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        if (gn + e < p.N) crow[gn + e] = v[e];
+                        if (gn + e < p.N && in_range(gn + e, p.N)) crow[gn + e] = v[e];
                 }
             }
         }

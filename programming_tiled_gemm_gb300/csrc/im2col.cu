@@ -14,6 +14,9 @@
 #include "internal.h"
 
 namespace gemm_gb300 {
+
+GEMM_DEBUG_UNIT(im2col)
+
 namespace {
 
 struct Im2colGeom {
@@ -23,6 +26,7 @@ struct Im2colGeom {
     int in1, in2, in3;         // input extents (in0 only enters through the channel stride)
     int p1, p2, p3;            // output extents
     int64_t chan_stride;       // in0*in1*in2*in3
+    int64_t x_elems;           // cin * chan_stride (index checks of debug builds)
 };
 
 // The position part of a column's source offset is the same for every row:
@@ -70,9 +74,12 @@ __global__ void __launch_bounds__(IM_THREADS) im2col4d_kernel(const float* __res
         const int r0 = (int)(t % g.k0);
         const int64_t c = t / g.k0;
         // input element of output position (0, 0, 0, 0) for this tap
-        const float* xb = x + c * g.chan_stride + (((int64_t)r0 * g.in1 + r1) * g.in2 + r2) * g.in3 + r3;
+        const int64_t xo = c * g.chan_stride + (((int64_t)r0 * g.in1 + r1) * g.in2 + r2) * g.in3 + r3;
+        const float* xb = x + xo;
         float* dst = col + row * (int64_t)g.ncols + n0;
+        if (!in_range(xo + o4.x, g.x_elems) || !in_range(xo + (n0 + 3 < g.ncols ? o4.w : o4.x), g.x_elems)) continue;
         if (QUAD) {
+            if (!in_range(n0 + 3, g.ncols)) continue;
             float4 v;
             v.x = __ldg(xb + o4.x);
             v.y = __ldg(xb + o4.y);
@@ -123,7 +130,11 @@ __global__ void __launch_bounds__(IM_THREADS) im2col4d_group_kernel(const float*
         t /= g.k1;
         const int r0 = (int)(t % g.k0);
         const int64_t c = t / g.k0;
-        const float* src = x + c * g.chan_stride + (((int64_t)r0 * g.in1 + r1) * g.in2 + r2) * g.in3 + o;
+        const int64_t xo = c * g.chan_stride + (((int64_t)r0 * g.in1 + r1) * g.in2 + r2) * g.in3 + o;
+        if (!in_range(xo, g.x_elems) || !in_range(xo + 7, g.x_elems) || !in_range(grp * g.k3 + 4, g.nrows) ||
+            !in_range(n0 + 3, g.ncols))
+            continue;
+        const float* src = x + xo;
         const float4 lo = __ldg(reinterpret_cast<const float4*>(src));
         const float4 hi = __ldg(reinterpret_cast<const float4*>(src + 4));
         const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
@@ -151,6 +162,7 @@ cudaError_t launch_im2col4d(const float* x, int64_t cin, const int64_t in[4], co
     g.p1 = (int)p1, g.p2 = (int)p2, g.p3 = (int)p3;
     g.chan_stride = in[0] * in[1] * in[2] * in[3];
     if (g.chan_stride >= (1ll << 31)) return cudaErrorInvalidValue;  // 32-bit position offsets
+    g.x_elems = cin * g.chan_stride;
     // blocks along x cover the columns once; along y they share the rows, about 16
     // blocks per SM in all
     const int64_t gx64 = (ncols + IM_COLS - 1) / IM_COLS;

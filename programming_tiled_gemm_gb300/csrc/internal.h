@@ -19,6 +19,57 @@ enum DeviceStatus : int {
     kDevTimeoutDrain = 4      // a CTA gave up draining its own copies / MMAs before exit
 };
 
+// ------------------------------------------------------------------ host-side log
+// With the environment variable GEMM_LOG=1 (read once per process) the library prints one
+// line per call on stderr: the kernel it chose, its split of K, the workspace it uses, and
+// the reason for every refused call.  Otherwise nothing is printed.
+bool log_enabled();
+void glog(const char* fmt, ...) __attribute__((format(printf, 1, 2)));
+
+// ------------------------------------------------------------------ debug builds
+// Built with -DGEMM_DEBUG (lib/libgemm_gb300_debug.so), every global access a kernel makes
+// through an index it computed is checked against the extent of its operand first: a check
+// that fails raises the bounds flag of the kernel's translation unit and the access is
+// skipped (no trap, no assert; the thread carries on, so every barrier is still reached).
+// gemm_get_device_status reads and clears the flags of all translation units and reports
+// GEMM_ERR_DEVICE_BOUNDS.  The flags belong to the process and the device, not to a handle.
+// In release builds in_range() is constant true and the checks compile away.
+#ifdef GEMM_DEBUG
+#define GEMM_DEBUG_UNIT(name)                                                                \
+    __device__ int g_bounds_flag_##name;                                                     \
+    int bounds_flag_take_##name()                                                            \
+    {                                                                                        \
+        int v = 0, z = 0;                                                                    \
+        if (cudaMemcpyFromSymbol(&v, g_bounds_flag_##name, sizeof(int)) != cudaSuccess) {     \
+            (void)cudaGetLastError();                                                        \
+            return -1;                                                                       \
+        }                                                                                    \
+        if (v && cudaMemcpyToSymbol(g_bounds_flag_##name, &z, sizeof(int)) != cudaSuccess) { \
+            (void)cudaGetLastError();                                                        \
+            return -1;                                                                       \
+        }                                                                                    \
+        return v;                                                                            \
+    }                                                                                        \
+    static __device__ __forceinline__ bool in_range(int64_t i, int64_t n)                   \
+    {                                                                                        \
+        const bool ok = i >= 0 && i < n;                                                     \
+        if (!ok) atomicExch(&g_bounds_flag_##name, 1);                                      \
+        return ok;                                                                           \
+    }
+// The translation units with kernels (each uses GEMM_DEBUG_UNIT once).
+int bounds_flag_take_ffma();
+int bounds_flag_take_ffma_tma();
+int bounds_flag_take_skinny();
+int bounds_flag_take_skinny_tma();
+int bounds_flag_take_im2col();
+int bounds_flag_take_conv_implicit();
+int bounds_flag_take_conv_tc();
+int bounds_flag_take_tc_gemm();
+#else
+#define GEMM_DEBUG_UNIT(name) \
+    static __device__ __forceinline__ constexpr bool in_range(int64_t, int64_t) { return true; }
+#endif
+
 // Output step of the generalised product: C = alpha * (A . B) + beta * C, C stored as
 // fp32, bf16 or fp16 (a gemm_dtype_t); C is not read when beta == 0.
 struct Epilogue {

@@ -17,6 +17,9 @@
 #include "internal.h"
 
 namespace gemm_gb300 {
+
+GEMM_DEBUG_UNIT(skinny)
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -64,7 +67,7 @@ skinny_kernel(F32Args p, int64_t k_per_split, float* ws, int vec_out)
             if (e < KB * MR) {
                 const int kk = e % KB, m = e / KB;
                 const int64_t gk = k0 + kk;
-                const bool ok = (m < p.M) && (gk < kend);
+                const bool ok = (m < p.M) && (gk < kend) && in_range(m, p.M) && in_range(gk, p.K);
                 const float* src = ok ? (p.A + (int64_t)m * p.lda + gk) : p.A;
                 cp_async_4(&As[buf][kk][m], src, ok ? 4 : 0);
             }
@@ -73,7 +76,7 @@ skinny_kernel(F32Args p, int64_t k_per_split, float* ws, int vec_out)
 
     auto load_b = [&](int64_t k) -> float4 {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (k < kend && col_ok) {
+        if (k < kend && col_ok && in_range(k, p.K) && in_range(col, p.N)) {
             const float* src = p.B + k * p.ldb + col;
             if (VEC && col_full) {
                 v = __ldg(reinterpret_cast<const float4*>(src));
@@ -139,7 +142,7 @@ skinny_kernel(F32Args p, int64_t k_per_split, float* ws, int vec_out)
     if (!col_ok) return;
 #pragma unroll
     for (int m = 0; m < MR; ++m) {
-        if (m >= p.M) break;
+        if (m >= p.M || !in_range(m, p.M) || !in_range(col, p.N)) break;
         float* dst = out + (int64_t)m * ldo + col;
         if (vec_out && col_full) {
             *reinterpret_cast<float4*>(dst) = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);

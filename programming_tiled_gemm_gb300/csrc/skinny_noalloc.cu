@@ -105,9 +105,8 @@ int scratch_for_current_device(DeviceScratch* out)
 
 using namespace gemm_gb300;
 
-extern "C" int gemm_run_f32_skinny_noalloc(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-                                           const float* B, int64_t ldb, float* C, int64_t ldc, int split_k,
-                                           void* stream)
+static int run_noalloc(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B, int64_t ldb,
+                       float* C, int64_t ldc, int split_k, void* stream)
 {
     if (split_k < 0 || split_k > 1024) return GEMM_ERR_INVALID_ARG;
     const int rc0 = check_product_args(M, N, K, A, lda, B, ldb, C, ldc);
@@ -126,7 +125,25 @@ extern "C" int gemm_run_f32_skinny_noalloc(int64_t M, int64_t N, int64_t K, cons
     if ((int64_t)split > K) split = (int)K;
     // every split slice is fully written before it is summed: nothing needs clearing
     // (compared by division: split * M * N itself may overflow for absurd N)
-    if (split > 1 && N > kScratchFloats / ((int64_t)split * M)) return GEMM_ERR_UNSUPPORTED;
+    if (split > 1 && N > kScratchFloats / ((int64_t)split * M)) {
+        glog("gemm_run_f32_skinny_noalloc: split %d x M %lld x N %lld floats exceed the %lld-float scratch array", split,
+             (long long)M, (long long)N, (long long)kScratchFloats);
+        return GEMM_ERR_UNSUPPORTED;
+    }
+    glog("gemm_run_f32_skinny_noalloc %lldx%lldx%lld: skinny kernel (registers), split %d, scratch %lld floats",
+         (long long)M, (long long)N, (long long)K, split, split > 1 ? (long long)split * M * N : 0ll);
     int launches = 0;
     return launch_skinny(a, split, s.ptr, s.num_sms, st, &launches) == cudaSuccess ? GEMM_OK : fail_cuda();
+}
+
+extern "C" int gemm_run_f32_skinny_noalloc(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                                           const float* B, int64_t ldb, float* C, int64_t ldc, int split_k,
+                                           void* stream)
+{
+    const int rc = run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, split_k, stream);
+    if (rc != GEMM_OK)
+        glog("gemm_run_f32_skinny_noalloc(M %lld, N %lld, K %lld, lda %lld, ldb %lld, ldc %lld, split %d) refused: %s (%d)",
+             (long long)M, (long long)N, (long long)K, (long long)lda, (long long)ldb, (long long)ldc, split_k,
+             gemm_status_string(rc), rc);
+    return rc;
 }

@@ -27,6 +27,9 @@
 #include "ptx.h"
 
 namespace gemm_gb300 {
+
+GEMM_DEBUG_UNIT(skinny_tma)
+
 namespace {
 
 constexpr int ST_BOX_COLS = 256;  // TMA box width (max 256 elements)
@@ -130,7 +133,9 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
                     const int e = lane + 32 * i;
                     const int kk = e % ST_KROWS, m = e / ST_KROWS;
                     const int gk = k0 + kk;
-                    av[i] = (m < a.M && gk < kend) ? __ldg(a.A + (int64_t)m * p.lda + gk) : 0.f;
+                    av[i] = (m < a.M && gk < kend && in_range(m, a.M) && in_range(gk, a.K))
+                                ? __ldg(a.A + (int64_t)m * p.lda + gk)
+                                : 0.f;
                 }
                 bool got = (lane == 0) ? mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.limit_ns, abort_flag)
                                        : true;
@@ -274,6 +279,7 @@ skinny_tma_kernel(const __grid_constant__ CUtensorMap tmB, StParams p)
 #pragma unroll
                 for (int m = 0; m < RT; ++m) {
                     if (m_base + m >= a.M) break;
+                    if (!in_range(m_base + m, a.M) || !in_range(col, a.N)) break;
                     float* dst = out + (int64_t)(m_base + m) * ldo + col;
                     float v[4];
 #pragma unroll

@@ -55,6 +55,9 @@
 #include "ptx.h"
 
 namespace gemm_gb300 {
+
+GEMM_DEBUG_UNIT(tc_gemm)
+
 namespace {
 
 constexpr int BM = 128;              // rows of an output tile (TMEM lanes)
@@ -287,6 +290,8 @@ __device__ __forceinline__ bool rem_slice_combine(const TcParams& p, float (&tot
                                                   int w, int lane, int* status, volatile int* abort_flag)
 {
     const int S = p.rem_split;
+    if (!in_range(j, p.num_tiles - p.rem_first) || !in_range(sl, S) || !in_range(cta, 2) || !in_range(w, EPI_WARPS))
+        return false;
     float* base = p.rem_ws + ((int64_t)(j * S) * 2 * EPI_WARPS + cta * EPI_WARPS + w) * REM_PART_FLOATS;
     const int64_t zstride = (int64_t)2 * EPI_WARPS * REM_PART_FLOATS;  // between slices
     float4* mine = reinterpret_cast<float4*>(base + sl * zstride) + lane;
@@ -976,6 +981,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // finish stores it, the second adds itself in L2 (a + b = b + a: the same
                 // bits whichever comes first)
                 const int64_t part = ((int64_t)(t - p.rem_first) * 2 + rank) * EPI_WARPS + (warp - 2);
+                if (!in_range(part, (int64_t)(p.num_tiles - p.rem_first) * 2 * EPI_WARPS)) continue;
                 int n = 0;
                 if (lane == 0) {
                     n = slice_arrive(p.rem_cnt + part, p.rem_seq);

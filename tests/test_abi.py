@@ -7,6 +7,7 @@ import ctypes
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 
@@ -132,3 +133,45 @@ def test_noalloc_entry_point_checks_sizes_before_touching_cuda(pkg):
     assert lib.gemm_run_f32_skinny_noalloc(33, 256, 64, p, 64, p, 256, p, 256, 0, None) == pkg.GEMM_ERR_UNSUPPORTED
     assert lib.gemm_run_f32_skinny_noalloc(16, 256, 64, p, 63, p, 256, p, 256, 0, None) == pkg.GEMM_ERR_INVALID_ARG
     assert lib.gemm_run_f32_skinny_noalloc(16, 256, 64, p, 64, p, 256, p, 256, 2000, None) == pkg.GEMM_ERR_INVALID_ARG
+
+
+def test_debug_library_exports_the_same_symbols(pkg):
+    """The debug build (kernels with index checks) exports the same C ABI."""
+    path = os.path.join(os.path.dirname(pkg.LIB_PATH), "libgemm_gb300_debug.so")
+    assert os.path.exists(path)
+    lib = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(lib, name), "missing export " + name
+
+
+LOG_PROBE = r"""
+import ctypes, sys
+lib = ctypes.CDLL(sys.argv[1])
+i64, p, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+lib.gemm_run_f32_skinny_noalloc.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, i32, p]
+lib.gemm_set_option.argtypes = [p, i32, i64]
+assert lib.gemm_run_f32_skinny_noalloc(33, 256, 64, 256, 64, 256, 256, 256, 256, 0, None) == -3
+assert lib.gemm_set_option(None, 1, 0) == -1
+"""
+
+
+def run_log_probe(pkg, env_extra):
+    env = {k: v for k, v in os.environ.items() if k != "GEMM_LOG"}
+    env.update(env_extra)
+    return subprocess.run([sys.executable, "-c", LOG_PROBE, pkg.LIB_PATH], capture_output=True, text=True, env=env,
+                          timeout=120)
+
+
+def test_gemm_log_reports_refused_calls_on_stderr(pkg):
+    p = run_log_probe(pkg, {"GEMM_LOG": "1"})
+    assert p.returncode == 0, p.stderr
+    lines = [ln for ln in p.stderr.splitlines() if ln.startswith("[gemm] ")]
+    assert any("gemm_run_f32_skinny_noalloc(M 33" in ln and "refused" in ln for ln in lines), p.stderr
+    assert any("gemm_set_option(1, 0) refused" in ln for ln in lines), p.stderr
+
+
+def test_without_gemm_log_nothing_is_printed(pkg):
+    for env in ({}, {"GEMM_LOG": "0"}, {"GEMM_LOG": "yes"}):
+        p = run_log_probe(pkg, env)
+        assert p.returncode == 0, p.stderr
+        assert p.stderr == "", p.stderr
