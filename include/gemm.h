@@ -204,16 +204,14 @@ int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t 
  * Products of 16-bit values are exact in fp32; the tensor core accumulates in fp32, with
  * consecutive MMAs (16 channels of one window of taps) going round-robin to up to 8
  * partial sums that are added in fp32 round-to-nearest, in order.  Deterministic.
- * Asynchronous on `stream`.  Two launches: one stages the input and the weights in the
- * handle's workspace (grown on demand, about the size of x plus the size of w times
- * (k[3] + 2S - 2) / k[3], S from GEMM_OPT_CONV_STACK), one computes y (a programmatic
- * dependent launch: it sets up while the first runs and waits for it before reading the
- * workspace).
+ * Asynchronous on `stream`.  One launch on CTA pairs (tcgen05 cta_group::2), reading x and w
+ * straight from the caller's tensors with the Tensor Memory Accelerator; no workspace.
  * x, w and y must be 16-byte aligned (GEMM_ERR_ALIGNMENT).
  * GEMM_ERR_INVALID_ARG for bad extents, pointers or dtype (GEMM_BF16 or GEMM_F16 only);
  * GEMM_ERR_UNSUPPORTED unless C_in % 16 == 0, C_out % 16 == 0, S * C_out <= 256,
- * in[3] % S == 0, and three pipeline stages of one filter triple (r0, r1, r2) fit in
- * shared memory. */
+ * in[3] % S == 0, three pipeline stages of one filter triple (r0, r1, r2) and one 16-channel
+ * step fit in shared memory, and the input rows of one stage (128 + (k[3] + S - 2) / S)
+ * are at most 256. */
 int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
                       int64_t C_out, const int64_t k_dims[4], float* y, int dtype, void* stream);
 

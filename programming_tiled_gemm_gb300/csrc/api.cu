@@ -699,10 +699,13 @@ static int conv4d_forward_cl_impl(gemm_handle_t h, const void* x, int64_t C_in, 
     if (!g.ok()) return GEMM_ERR_CUDA;
     const int64_t ws = conv4d_tc_workspace(C_in, in_dims, C_out, k_dims, h->opt_conv_stack);
     if (ws < 0) return GEMM_ERR_UNSUPPORTED;
-    int rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, (size_t)ws);
-    if (rc != GEMM_OK) return rc;
-    glog("conv4d_forward_cl: tensor-core convolution, staged operands %lld bytes (stack option %d)", (long long)ws,
-         h->opt_conv_stack);
+    int rc = GEMM_OK;
+    if (ws > 0) {
+        rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, (size_t)ws);
+        if (rc != GEMM_OK) return rc;
+    }
+    glog("conv4d_forward_cl: tensor-core convolution on CTA pairs, workspace %lld bytes (stack option %d)",
+         (long long)ws, h->opt_conv_stack);
     int n = 0;
     rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, dtype == GEMM_BF16, h->opt_conv_stack, h->workspace,
                           h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall,

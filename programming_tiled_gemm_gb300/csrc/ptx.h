@@ -312,7 +312,9 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 //   K-major, 128-byte swizzle: rows of 128 bytes in 1024-byte atoms of 8 rows (atoms
 //     1024-byte aligned); SBO = bytes between atoms along M/N; a start address moved by
 //     32 bytes selects the next 16 elements of K inside the atom.
-constexpr uint32_t kLayoutNoSwizzle = 0, kLayoutSwizzle128 = 2;
+//   K-major, 32-byte swizzle: rows of 32 bytes (16 16-bit elements of K) in 256-byte atoms
+//     of 8 rows; SBO = bytes between atoms along M/N.
+constexpr uint32_t kLayoutNoSwizzle = 0, kLayoutSwizzle128 = 2, kLayoutSwizzle32 = 6;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint32_t layout)
@@ -329,6 +331,129 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
 {
     return smem_desc(saddr, lbo_bytes, sbo_bytes, kLayoutSwizzle128);
+}
+
+// ------------------------------------------------------------------ CTA pairs (cta_group::2)
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait (acquire at cluster scope); gives up early once `abort_flag` is set.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                  volatile int* abort_flag)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((abort_flag && *abort_flag) || global_timer() - t0 > limit_ns) return false;
+    }
+}
+
+// The same wait for long waits: sleeps `sleep_ns` between polls, so that the waiting warp
+// leaves its scheduler's issue slots to the warps doing the work.
+__device__ __forceinline__ bool mbar_wait_cluster_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                        volatile int* abort_flag, unsigned sleep_ns)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    while (true) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((abort_flag && *abort_flag) || global_timer() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same load with an L2 eviction-priority policy.
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                      int x, int y, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(pol)
+        : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on a barrier that
+// may live in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Arrive on the barrier at this offset in every CTA of `mask` once every tcgen05.mma
+// issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_mask(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(bar), "h"(mask)
+        : "memory");
+}
+
+// Spin (bounded by wall clock) so that copies and MMAs still in flight after an abort
+// can land before shared memory is released.
+__device__ __forceinline__ void grace_period(uint64_t ns)
+{
+    const uint64_t t0 = global_timer();
+    while (global_timer() - t0 < ns) {
+    }
+}
+
+// 4-D tiled load for a CTA pair (coordinates innermost first); completes on a barrier
+// that may live in the peer CTA (cluster address).  Out-of-range boxes read zeros.
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                 int c1, int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
 }
 
 }  // namespace gemm_gb300

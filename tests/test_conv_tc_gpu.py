@@ -154,8 +154,14 @@ def test_argument_errors_are_reported(lib):
     assert run(h, x.data_ptr(), 16, ins, x.data_ptr(), 16, ks, y.data_ptr(), g.GEMM_F32) == g.GEMM_ERR_INVALID_ARG
     assert run(h, x.data_ptr(), 16, ins, x.data_ptr(), 16, [1, 1, 5, 2], y.data_ptr(),
                g.GEMM_BF16) == g.GEMM_ERR_INVALID_ARG
-    # one filter triple's weights do not fit three pipeline stages
-    assert run(h, x.data_ptr(), 512, [2, 2, 4, 8], x.data_ptr(), 128, [1, 1, 1, 4], y.data_ptr(),
+    # (every call below is refused before anything is launched: the buffers are far smaller
+    # than the shapes they stand for)
+    # one filter triple's weights for one 16-channel step (2 boxes of 20 slices x 128
+    # channels x 16 bytes) do not fit three pipeline stages; N = 2 C_out > 256 rules out S = 2
+    assert run(h, x.data_ptr(), 16, [1, 1, 2, 24], x.data_ptr(), 256, [1, 1, 1, 20], y.data_ptr(),
+               g.GEMM_BF16) == g.GEMM_ERR_UNSUPPORTED
+    # a filter row longer than one input box reaches (more than 256 rows of S positions)
+    assert run(h, x.data_ptr(), 16, [1, 1, 1, 258], x.data_ptr(), 16, [1, 1, 1, 258], y.data_ptr(),
                g.GEMM_BF16) == g.GEMM_ERR_UNSUPPORTED
     # a stack that does not divide in[3], or makes N = S C_out wider than 256
     lib.set_option(g.GEMM_OPT_CONV_STACK, 4)
