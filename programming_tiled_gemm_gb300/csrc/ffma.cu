@@ -531,6 +531,38 @@ splitk_reduce_kernel(const float* __restrict__ ws, int split, int64_t M, int64_t
     }
 }
 
+// The same sum for rows of a multiple of four floats: four adjacent outputs per thread and
+// the partials of four slices in flight at once; the additions keep the slice order.
+__global__ void __launch_bounds__(256)
+splitk_reduce4_kernel(const float* __restrict__ ws, int split, int64_t M, int64_t N,
+                      float* __restrict__ C, int64_t ldc)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the partials' writer has finished
+    const int64_t total = M * N;
+    const int64_t n4 = N / 4;
+    const int64_t quads = M * n4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += stride) {
+        const int64_t m = q / n4, n = (q - m * n4) * 4;
+        if (!in_range(m, M) || !in_range(n + 3, N)) continue;
+        const float* src = ws + q * 4;
+        float4 s = __ldcs(reinterpret_cast<const float4*>(src));
+        int z = 1;
+        for (; z + 4 <= split; z += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = __ldcs(reinterpret_cast<const float4*>(src + (int64_t)(z + u) * total));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s.x += v[u].x, s.y += v[u].y, s.z += v[u].z, s.w += v[u].w;
+        }
+        for (; z < split; ++z) {
+            const float4 v = __ldcs(reinterpret_cast<const float4*>(src + (int64_t)z * total));
+            s.x += v.x, s.y += v.y, s.z += v.z, s.w += v.w;
+        }
+        *reinterpret_cast<float4*>(C + m * ldc + n) = s;
+    }
+}
+
 // C = alpha * P + beta * C (C unread when beta == 0), stored as fp32, bf16 or fp16.
 // P == nullptr stands for a zero product.
 template <int CT>
@@ -724,11 +756,16 @@ cudaError_t launch_epilogue(const float* P, int64_t ldp, void* C, int64_t ldc, i
 cudaError_t launch_splitk_reduce(const float* ws, int split, int64_t M, int64_t N, float* C,
                                  int64_t ldc, int num_sms, cudaStream_t stream)
 {
-    const int64_t total = M * N;
+    const bool vec4 = N % 4 == 0 && ldc % 4 == 0 &&
+                      ((reinterpret_cast<uintptr_t>(ws) | reinterpret_cast<uintptr_t>(C)) & 15) == 0;
+    const int64_t total = vec4 ? M * (N / 4) : M * N;
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 152) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    if (vec4)
+        return launch_dependent(splitk_reduce4_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, ws, split, M, N,
+                                C, ldc);
     return launch_dependent(splitk_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, ws, split, M, N, C,
                             ldc);
 }
