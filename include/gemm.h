@@ -215,6 +215,29 @@ int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t 
 int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
                       int64_t C_out, const int64_t k_dims[4], float* y, int dtype, void* stream);
 
+/* The tensor-core convolution for 16-bit operands in PyTorch's channel-first order
+ * ("Three X: large convolutions in PyTorch for training", section "CUTLASS", its closing
+ * part on memory layout: PyTorch keeps channels outermost, so the channel-last operands
+ * the tensor-core implicit GEMM wants are produced by transposing the input and the
+ * filters first).
+ *   x : [C_in][in[0]][in[1]][in[2]][in[3]], bf16 or fp16 (`dtype`), contiguous, device.
+ *   w : [C_out][C_in][k[0]][k[1]][k[2]][k[3]], the same type, contiguous, device.
+ *   y : fp32 output, y[o][p] at y + o*ldy + p (the layout of conv4d_forward), p the
+ *       row-major output position over (P0, P1, P2, P3), Pd = in[d] - k[d] + 1;
+ *       ldy >= P0*P1*P2*P3.  Overwritten.
+ * Three launches on `stream`: x and w are re-laid channel-last into the handle's
+ * workspace (V*Cp + C_out*T*Cp 16-bit values, V = in[0]*..*in[3], T = k[0]*..*k[3],
+ * Cp = C_in rounded up to a multiple of 16, the added channels zero), then the kernel of
+ * conv4d_forward_cl runs on those copies and stores y channel-first.  Results equal
+ * conv4d_forward_cl's on the re-laid operands, bit for bit.
+ * x and w must be 2-byte aligned and y 4-byte aligned (GEMM_ERR_ALIGNMENT).
+ * GEMM_ERR_INVALID_ARG for bad extents, pointers, ldy or dtype (GEMM_BF16 or GEMM_F16);
+ * GEMM_ERR_UNSUPPORTED when conv4d_forward_cl would refuse C_in = Cp (C_out % 16 != 0,
+ * S * C_out > 256, a stage that does not fit) or the copies' sizes leave 64 bits;
+ * GEMM_ERR_CUDA if the workspace cannot be allocated. */
+int conv4d_forward_tc(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
+                      int64_t C_out, const int64_t k_dims[4], float* y, int64_t ldy, int dtype, void* stream);
+
 /* Synchronise `stream`, then read and clear the handle's device status word (and, in the
  * debug library, the kernels' bounds-check flags).  This is
  * the wait of "Learning to develop for GPU with GEMM as the example", section "Writing a

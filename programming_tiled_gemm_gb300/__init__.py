@@ -31,7 +31,7 @@ GEMM_OPT_CONV_STACK = 7
 # Every symbol include/gemm.h declares (the ABI test checks the library exports them).
 EXPORTS = ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host", "gemm_run_host_batch",
            "conv4d_im2col",
-           "conv4d_forward", "conv4d_forward_cl",
+           "conv4d_forward", "conv4d_forward_cl", "conv4d_forward_tc",
            "gemm_get_device_status", "gemm_set_option", "gemm_launch_count", "gemm_status_string",
            "gemm_run_f32_skinny_noalloc"]
 
@@ -64,6 +64,7 @@ def _load():
     lib.conv4d_im2col.argtypes = [p, p, i64, ctypes.POINTER(i64), ctypes.POINTER(i64), p, p]
     lib.conv4d_forward.argtypes = [p, p, i64, ctypes.POINTER(i64), p, i64, ctypes.POINTER(i64), p, i64, p]
     lib.conv4d_forward_cl.argtypes = [p, p, i64, ctypes.POINTER(i64), p, i64, ctypes.POINTER(i64), p, i32, p]
+    lib.conv4d_forward_tc.argtypes = [p, p, i64, ctypes.POINTER(i64), p, i64, ctypes.POINTER(i64), p, i64, i32, p]
     lib.gemm_get_device_status.argtypes = [p, p]
     lib.gemm_set_option.argtypes = [p, i32, i64]
     lib.gemm_launch_count.argtypes = [p]
@@ -133,6 +134,12 @@ def conv4d_forward_cl(h, x, C_in, in_dims, w, C_out, k_dims, y, dtype, stream=0)
     ins = (ctypes.c_int64 * 4)(*[int(v) for v in in_dims])
     ks = (ctypes.c_int64 * 4)(*[int(v) for v in k_dims])
     return _lib.conv4d_forward_cl(h, x, C_in, ins, w, C_out, ks, y, dtype, stream)
+
+
+def conv4d_forward_tc(h, x, C_in, in_dims, w, C_out, k_dims, y, ldy, dtype, stream=0) -> int:
+    ins = (ctypes.c_int64 * 4)(*[int(v) for v in in_dims])
+    ks = (ctypes.c_int64 * 4)(*[int(v) for v in k_dims])
+    return _lib.conv4d_forward_tc(h, x, C_in, ins, w, C_out, ks, y, ldy, dtype, stream)
 
 
 def gemm_get_device_status(h, stream=0) -> int:
@@ -322,6 +329,37 @@ class Gemm:
             raise GemmError(rc, "conv4d_forward_cl")
         return out
 
+    def conv4d_tc(self, x, w, out=None, stream=None):
+        """Valid 4-D cross-correlation on the tensor cores, channel-first 16-bit operands.
+
+        x: [C_in, I0, I1, I2, I3] and w: [C_out, C_in, R0, R1, R2, R3], both bf16 or both
+        fp16, contiguous; returns y: fp32 [C_out, P0, P1, P2, P3] (or writes `out`, whose
+        rows over the output positions may be strided: out[o] at out.data_ptr() + o
+        out.stride(0))."""
+        import torch
+        dt = {torch.bfloat16: GEMM_BF16, torch.float16: GEMM_F16}.get(x.dtype)
+        if x.dim() != 5 or w.dim() != 6 or dt is None or w.dtype != x.dtype:
+            raise ValueError("x must be [C_in, I0..I3] and w [C_out, C_in, R0..R3], both bf16 or both fp16")
+        if not (x.is_contiguous() and w.is_contiguous()) or w.shape[1] != x.shape[0]:
+            raise ValueError("x and w must be contiguous with the same C_in")
+        cin, cout = x.shape[0], w.shape[0]
+        ins, ks = list(x.shape[1:]), list(w.shape[2:])
+        outs = [i - k + 1 for i, k in zip(ins, ks)]
+        npos = 1
+        for v in outs:
+            npos *= v
+        if out is None:
+            out = torch.empty([cout] + outs, dtype=torch.float32, device=x.device)
+        if out.dtype != torch.float32 or out.shape[0] != cout or out[0].numel() != npos or \
+                not out[0].is_contiguous():
+            raise ValueError("out must be fp32 [%d, %s] with contiguous rows" % (cout, outs))
+        s = torch.cuda.current_stream(x.device).cuda_stream if stream is None else int(stream)
+        rc = conv4d_forward_tc(self.handle, x.data_ptr(), cin, ins, w.data_ptr(), cout, ks, out.data_ptr(),
+                               out.stride(0), dt, s)
+        if rc != GEMM_OK:
+            raise GemmError(rc, "conv4d_forward_tc")
+        return out
+
     def conv4d(self, x, w, col=None, out=None, stream=None):
         """Valid 4-D cross-correlation as im2col + GEMM: y[C_out, P0, P1, P2, P3]."""
         ks = list(w.shape[2:])
@@ -342,6 +380,6 @@ class Gemm:
 
 __all__ = ["Gemm", "GemmError", "HostProblem", "gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex",
            "gemm_run_host", "gemm_run_host_batch",
-           "conv4d_im2col", "conv4d_forward", "conv4d_forward_cl", "gemm_get_device_status", "gemm_set_option", "gemm_launch_count",
+           "conv4d_im2col", "conv4d_forward", "conv4d_forward_cl", "conv4d_forward_tc", "gemm_get_device_status", "gemm_set_option", "gemm_launch_count",
            "gemm_status_string",
            "status_string", "library", "LIB_PATH", "EXPORTS"]

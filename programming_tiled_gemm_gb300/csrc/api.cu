@@ -707,9 +707,57 @@ static int conv4d_forward_cl_impl(gemm_handle_t h, const void* x, int64_t C_in, 
     glog("conv4d_forward_cl: tensor-core convolution on CTA pairs, workspace %lld bytes (stack option %d)",
          (long long)ws, h->opt_conv_stack);
     int n = 0;
-    rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, dtype == GEMM_BF16, h->opt_conv_stack, h->workspace,
+    rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, 0, dtype == GEMM_BF16, h->opt_conv_stack, h->workspace,
                           h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall,
                           reinterpret_cast<cudaStream_t>(stream), &n);
+    h->launches += n;
+    return rc;
+}
+
+static int conv4d_forward_tc_impl(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
+                                  int64_t C_out, const int64_t k_dims[4], float* y, int64_t ldy, int dtype,
+                                  void* stream)
+{
+    if (!h || !x || !w || !y || !in_dims || !k_dims || C_in <= 0 || C_out <= 0) return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_BF16 && dtype != GEMM_F16) return GEMM_ERR_INVALID_ARG;
+    int64_t V = 1, T = 1, npos = 1;
+    for (int d = 0; d < 4; ++d) {
+        if (in_dims[d] <= 0 || k_dims[d] <= 0 || k_dims[d] > in_dims[d] || in_dims[d] > (1 << 20))
+            return GEMM_ERR_INVALID_ARG;
+        // each factor is at most 2^20: stop before the products can leave 64 bits
+        if (V > (1ll << 40) || T > (1ll << 40)) return GEMM_ERR_UNSUPPORTED;
+        V *= in_dims[d];
+        T *= k_dims[d];
+        npos *= in_dims[d] - k_dims[d] + 1;
+    }
+    if (C_in > (1 << 20) || C_out > (1 << 20) || ldy < npos) return GEMM_ERR_INVALID_ARG;
+    if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w)) & 1) != 0 ||
+        (reinterpret_cast<uintptr_t>(y) & 3) != 0)
+        return GEMM_ERR_ALIGNMENT;
+    const int64_t Cp = (C_in + 15) / 16 * 16;  // channels padded to the MMA's K with zeros
+    if (V > (1ll << 40) || T > (1ll << 40) || (double)V * Cp >= 9.0e15 || (double)C_out * T * Cp >= 9.0e15)
+        return GEMM_ERR_UNSUPPORTED;
+    if (conv4d_tc_workspace(Cp, in_dims, C_out, k_dims, h->opt_conv_stack) < 0) return GEMM_ERR_UNSUPPORTED;
+    DeviceGuard g(h->device);
+    if (!g.ok()) return GEMM_ERR_CUDA;
+    // channel-last copies of x and w in the workspace, each on a 256-byte boundary
+    const size_t x_bytes = (size_t)(V * Cp * 2 + 255) / 256 * 256;
+    const size_t w_bytes = (size_t)(C_out * T * Cp * 2);
+    int rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, x_bytes + w_bytes);
+    if (rc != GEMM_OK) return rc;
+    void* xc = h->workspace;
+    void* wc = reinterpret_cast<uint8_t*>(h->workspace) + x_bytes;
+    glog("conv4d_forward_tc: channel-first %s operands re-laid channel-last (C_in %lld padded to %lld), "
+         "workspace %lld bytes, then the tensor-core convolution with channel-first output",
+         dtype_name(dtype), (long long)C_in, (long long)Cp, (long long)(x_bytes + w_bytes));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_to_channel_last(x, 1, C_in, V, Cp, xc, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    h->launches += 1;
+    if (launch_to_channel_last(w, C_out, C_in, T, Cp, wc, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    h->launches += 1;
+    int n = 0;
+    rc = launch_conv4d_tc(xc, Cp, in_dims, wc, C_out, k_dims, y, ldy, dtype == GEMM_BF16, h->opt_conv_stack,
+                          h->workspace, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, s, &n);
     h->launches += n;
     return rc;
 }
@@ -817,6 +865,16 @@ int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_
     if (rc != GEMM_OK)
         glog("conv4d_forward_cl(C_in %lld, C_out %lld, %s) refused: %s (%d)", (long long)C_in, (long long)C_out,
              dtype_name(dtype), gemm_status_string(rc), rc);
+    return rc;
+}
+
+int conv4d_forward_tc(gemm_handle_t h, const void* x, int64_t C_in, const int64_t in_dims[4], const void* w,
+                      int64_t C_out, const int64_t k_dims[4], float* y, int64_t ldy, int dtype, void* stream)
+{
+    const int rc = conv4d_forward_tc_impl(h, x, C_in, in_dims, w, C_out, k_dims, y, ldy, dtype, stream);
+    if (rc != GEMM_OK)
+        glog("conv4d_forward_tc(C_in %lld, C_out %lld, ldy %lld, %s) refused: %s (%d)", (long long)C_in,
+             (long long)C_out, (long long)ldy, dtype_name(dtype), gemm_status_string(rc), rc);
     return rc;
 }
 

@@ -90,6 +90,7 @@ struct ConvTcParams {
     int tmem_cols;
     uint32_t idesc;
     float* y;
+    int64_t ldy_cf;     // 0: y channel-last [P][C_out]; else y channel-first, y[o][p] at y + o ldy_cf + p
     int* status;
     uint64_t limit_ns;
     int test_stall;
@@ -357,9 +358,17 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
                     const int p1 = u / plane, rem = u - p1 * plane;
                     const int p2 = rem / p.I[3], p3 = rem - p2 * p.I[3];
                     if (p1 < p.P[1] && p2 < p.P[2] && p3 < p.P[3] && in_range(p0, p.P[0]) && in_range(o + 7, p.cout)) {
-                        float* yrow = p.y + ((((int64_t)p0 * p.P[1] + p1) * p.P[2] + p2) * p.P[3] + p3) * p.cout + o;
-                        *reinterpret_cast<float4*>(yrow) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                        *reinterpret_cast<float4*>(yrow + 4) = make_float4(acc[j + 4], acc[j + 5], acc[j + 6], acc[j + 7]);
+                        const int64_t pos = (((int64_t)p0 * p.P[1] + p1) * p.P[2] + p2) * p.P[3] + p3;
+                        if (p.ldy_cf == 0) {
+                            float* yrow = p.y + pos * p.cout + o;
+                            *reinterpret_cast<float4*>(yrow) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                            *reinterpret_cast<float4*>(yrow + 4) =
+                                make_float4(acc[j + 4], acc[j + 5], acc[j + 6], acc[j + 7]);
+                        } else {
+                            float* ycol = p.y + (int64_t)o * p.ldy_cf + pos;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) ycol[(int64_t)e * p.ldy_cf] = acc[j + e];
+                        }
                     }
                 }
             }
@@ -375,6 +384,35 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, (uint32_t)p.tmem_cols);
+    }
+}
+
+// Channel-first to channel-last re-layout of 16-bit tensors for the channel-first entry
+// point: src [B][C][V] -> dst [B][V][Cp], channels C .. Cp-1 zero-filled.  A 32 x 32 tile
+// goes through shared memory so that both the reads along V and the writes along C are
+// coalesced.
+__global__ void __launch_bounds__(256)
+to_channel_last_kernel(const uint16_t* __restrict__ src, int64_t B, int64_t C, int64_t V, int64_t Cp,
+                       uint16_t* __restrict__ dst)
+{
+    __shared__ uint16_t tile[32][33];
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+    const int64_t v0 = (int64_t)blockIdx.x * 32, c0 = (int64_t)blockIdx.y * 32;
+    for (int64_t b = blockIdx.z; b < B; b += gridDim.z) {
+        const uint16_t* s = src + b * C * V;
+        uint16_t* d = dst + b * V * Cp;
+#pragma unroll
+        for (int i = ty; i < 32; i += 8) {
+            const int64_t c = c0 + i, v = v0 + tx;
+            tile[i][tx] = (c < C && v < V && in_range(c * V + v, C * V)) ? s[c * V + v] : (uint16_t)0;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = ty; i < 32; i += 8) {
+            const int64_t v = v0 + i, c = c0 + tx;
+            if (v < V && c < Cp && in_range(v * Cp + c, V * Cp)) d[v * Cp + c] = tile[tx][i];
+        }
+        __syncthreads();
     }
 }
 
@@ -514,8 +552,8 @@ int64_t conv4d_tc_workspace(int64_t cin, const int64_t in[4], int64_t cout, cons
 }
 
 int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void* w, int64_t cout,
-                     const int64_t k[4], float* y, bool bf16, int S, void* /*workspace*/, int num_sms, int* dev_status,
-                     uint64_t limit_ns, int test_stall, cudaStream_t stream, int* launches)
+                     const int64_t k[4], float* y, int64_t ldy_cf, bool bf16, int S, void* /*workspace*/, int num_sms,
+                     int* dev_status, uint64_t limit_ns, int test_stall, cudaStream_t stream, int* launches)
 {
     (void)num_sms;
     if (S <= 0) S = choose_stack(cin, in, cout, k);
@@ -525,6 +563,7 @@ int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void
     if (rc != GEMM_OK) return rc;
     p.idesc = conv_idesc(bf16, S * p.cout);
     p.y = y;
+    p.ldy_cf = ldy_cf;
     p.status = dev_status;
     p.limit_ns = limit_ns;
     p.test_stall = test_stall;
@@ -548,6 +587,18 @@ int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void
     if (cudaLaunchKernelEx(&cfg, conv4d_tc_pair_kernel, tmX, tmW, p) != cudaSuccess) return GEMM_ERR_CUDA;
     *launches += 1;
     return GEMM_OK;
+}
+
+cudaError_t launch_to_channel_last(const void* src, int64_t B, int64_t C, int64_t V, int64_t Cp, void* dst,
+                                   cudaStream_t stream)
+{
+    if (B <= 0 || C <= 0 || V <= 0 || Cp < C) return cudaErrorInvalidValue;
+    const int64_t gx = (V + 31) / 32, gy = (Cp + 31) / 32;
+    if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)(B < 65535 ? B : 65535));
+    to_channel_last_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(src), B, C, V, Cp,
+                                                     static_cast<uint16_t*>(dst));
+    return cudaGetLastError();
 }
 
 }  // namespace gemm_gb300

@@ -62,7 +62,7 @@ for pair, (M, N, K) in [(2, (520, 264, 136)), (0, (1024, 2048, 4096)), (1, (300,
           oracle.gemm(A.float().numpy(), B.float().numpy()))
 lib.set_option(g.GEMM_OPT_TC_PAIR, 0)
 
-# convolution: im2col, implicit GEMM, tensor cores (channel-last bf16)
+# convolution: im2col, implicit GEMM, tensor cores (channel-last bf16, then channel-first)
 gen = si.generator(7)
 x = si.ints((3, 6, 5, 7, 12), gen).float()
 w = si.ints((4, 3, 2, 1, 3, 5), gen).float()
@@ -74,6 +74,11 @@ w = si.ints((32, 16, 3, 3, 3, 3), gen).float()
 xc, wc = si.channel_last(x, w, "bf16")
 ref = np.ascontiguousarray(np.moveaxis(oracle.conv4d_direct(x.numpy(), w.numpy()), 0, -1))
 check("conv tensor cores", lib.conv4d_cl(xc.to(dev), wc.to(dev)), ref)
+gen = si.generator(9)
+x = si.ints((3, 6, 5, 7, 12), gen).float()
+w = si.ints((16, 3, 2, 1, 3, 5), gen).float()
+check("conv tensor cores, channel-first", lib.conv4d_tc(x.to(torch.bfloat16).to(dev), w.to(torch.bfloat16).to(dev)),
+      oracle.conv4d_direct(x.numpy(), w.numpy()))
 lib.close()
 print("debug build ok:", len(ran), "products")
 """
@@ -85,4 +90,4 @@ def test_debug_build_runs_every_kernel_family_without_a_failed_check():
     env = dict(os.environ, GEMM_GB300_DEBUG="1", PYTHONPATH=ROOT + os.pathsep + os.environ.get("PYTHONPATH", ""))
     p = subprocess.run([sys.executable, "-c", CHILD], capture_output=True, text=True, env=env, cwd=ROOT, timeout=900)
     assert p.returncode == 0, p.stdout + p.stderr
-    assert "debug build ok: 18 products" in p.stdout, p.stdout + p.stderr
+    assert "debug build ok: 19 products" in p.stdout, p.stdout + p.stderr
