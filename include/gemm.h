@@ -225,10 +225,12 @@ int conv4d_forward_cl(gemm_handle_t h, const void* x, int64_t C_in, const int64_
  *   y : fp32 output, y[o][p] at y + o*ldy + p (the layout of conv4d_forward), p the
  *       row-major output position over (P0, P1, P2, P3), Pd = in[d] - k[d] + 1;
  *       ldy >= P0*P1*P2*P3.  Overwritten.
- * Three launches on `stream`: x and w are re-laid channel-last into the handle's
+ * Two launches on `stream`: one kernel re-lays x and w channel-last into the handle's
  * workspace (V*Cp + C_out*T*Cp 16-bit values, V = in[0]*..*in[3], T = k[0]*..*k[3],
  * Cp = C_in rounded up to a multiple of 16, the added channels zero), then the kernel of
- * conv4d_forward_cl runs on those copies and stores y channel-first.  Results equal
+ * conv4d_forward_cl, launched as its programmatic dependent (its set-up overlaps the
+ * re-layout; its first copy waits for it), runs on those copies and stores y
+ * channel-first.  Results equal
  * conv4d_forward_cl's on the re-laid operands, bit for bit.
  * x and w must be 2-byte aligned and y 4-byte aligned (GEMM_ERR_ALIGNMENT).
  * GEMM_ERR_INVALID_ARG for bad extents, pointers, ldy or dtype (GEMM_BF16 or GEMM_F16);

@@ -708,7 +708,7 @@ static int conv4d_forward_cl_impl(gemm_handle_t h, const void* x, int64_t C_in, 
          (long long)ws, h->opt_conv_stack);
     int n = 0;
     rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, 0, dtype == GEMM_BF16, h->opt_conv_stack, h->workspace,
-                          h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall,
+                          h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, false,
                           reinterpret_cast<cudaStream_t>(stream), &n);
     h->launches += n;
     return rc;
@@ -751,13 +751,11 @@ static int conv4d_forward_tc_impl(gemm_handle_t h, const void* x, int64_t C_in, 
          "workspace %lld bytes, then the tensor-core convolution with channel-first output",
          dtype_name(dtype), (long long)C_in, (long long)Cp, (long long)(x_bytes + w_bytes));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_to_channel_last(x, 1, C_in, V, Cp, xc, s) != cudaSuccess) return GEMM_ERR_CUDA;
-    h->launches += 1;
-    if (launch_to_channel_last(w, C_out, C_in, T, Cp, wc, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (launch_to_channel_last(x, C_in, V, xc, w, C_out, T, wc, Cp, s) != cudaSuccess) return GEMM_ERR_CUDA;
     h->launches += 1;
     int n = 0;
     rc = launch_conv4d_tc(xc, Cp, in_dims, wc, C_out, k_dims, y, ldy, dtype == GEMM_BF16, h->opt_conv_stack,
-                          h->workspace, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, s, &n);
+                          h->workspace, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, true, s, &n);
     h->launches += n;
     return rc;
 }

@@ -165,6 +165,9 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     if (warp == 0) {
         // ---------------------------------------------------------------- producer (both CTAs)
         if (lane == 0) {
+            // after a programmatic launch (the channel-first re-layout): its output is complete
+            // and visible before the first copy (a no-op after an ordinary launch)
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             uint32_t issued_mask = 0, last_parity = 0;
             int slot = 0, r0 = 0, r1 = 0, grp = 0, kg = 0;
             uint32_t ph = 0;
@@ -388,32 +391,45 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
 }
 
 // Channel-first to channel-last re-layout of 16-bit tensors for the channel-first entry
-// point: src [B][C][V] -> dst [B][V][Cp], channels C .. Cp-1 zero-filled.  A 32 x 32 tile
-// goes through shared memory so that both the reads along V and the writes along C are
-// coalesced.
-__global__ void __launch_bounds__(256)
-to_channel_last_kernel(const uint16_t* __restrict__ src, int64_t B, int64_t C, int64_t V, int64_t Cp,
-                       uint16_t* __restrict__ dst)
+// point: src [B][C][V] -> dst [B][V][Cp], channels C .. Cp-1 zero-filled (Cp a multiple of
+// 16).  One launch does two independent jobs (the input, then the filters): the first
+// `blocks0` blocks belong to the first job.  Within a job, row (b, 8-channel chunk) is split
+// into blocks of 256 positions; a thread gathers the eight channels of one position (a
+// warp's reads of one channel are 32 consecutive positions) and stores them as one 16-byte
+// vector.
+struct RelayoutJob {
+    const uint16_t* src;
+    uint16_t* dst;
+    int64_t B, C, V, Cp;
+    int64_t blocks_per_row;  // ceil(V / 256)
+};
+
+__global__ void __launch_bounds__(256) to_channel_last_kernel(RelayoutJob j0, RelayoutJob j1, int64_t blocks0)
 {
-    __shared__ uint16_t tile[32][33];
-    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
-    const int64_t v0 = (int64_t)blockIdx.x * 32, c0 = (int64_t)blockIdx.y * 32;
-    for (int64_t b = blockIdx.z; b < B; b += gridDim.z) {
-        const uint16_t* s = src + b * C * V;
-        uint16_t* d = dst + b * V * Cp;
+    // the convolution launched next may set up (barriers, TMEM) now; its loads wait for this grid
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const bool first = blockIdx.x < blocks0;
+    const RelayoutJob& j = first ? j0 : j1;
+    const int64_t local = first ? (int64_t)blockIdx.x : (int64_t)blockIdx.x - blocks0;
+    const int64_t row = local / j.blocks_per_row;
+    const int64_t v = (local - row * j.blocks_per_row) * 256 + threadIdx.x;
+    const int64_t chunks = j.Cp / 8;
+    const int64_t b = row / chunks, c0 = (row - b * chunks) * 8;
+    if (v >= j.V || b >= j.B) return;
+    const uint16_t* s = j.src + b * j.C * j.V + v;
+    uint16_t e[8];
 #pragma unroll
-        for (int i = ty; i < 32; i += 8) {
-            const int64_t c = c0 + i, v = v0 + tx;
-            tile[i][tx] = (c < C && v < V && in_range(c * V + v, C * V)) ? s[c * V + v] : (uint16_t)0;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int i = ty; i < 32; i += 8) {
-            const int64_t v = v0 + i, c = c0 + tx;
-            if (v < V && c < Cp && in_range(v * Cp + c, V * Cp)) d[v * Cp + c] = tile[tx][i];
-        }
-        __syncthreads();
+    for (int i = 0; i < 8; ++i) {
+        const int64_t c = c0 + i;
+        e[i] = (c < j.C && in_range(b * j.C * j.V + c * j.V + v, j.B * j.C * j.V)) ? s[c * j.V] : (uint16_t)0;
     }
+    if (!in_range(b * j.V * j.Cp + v * j.Cp + c0 + 7, j.B * j.V * j.Cp)) return;
+    uint4 pk;
+    pk.x = (uint32_t)e[0] | ((uint32_t)e[1] << 16);
+    pk.y = (uint32_t)e[2] | ((uint32_t)e[3] << 16);
+    pk.z = (uint32_t)e[4] | ((uint32_t)e[5] << 16);
+    pk.w = (uint32_t)e[6] | ((uint32_t)e[7] << 16);
+    *reinterpret_cast<uint4*>(j.dst + b * j.V * j.Cp + v * j.Cp + c0) = pk;
 }
 
 // Tensor maps over the caller's channel-last tensors (16-bit elements, box rows of 8
@@ -553,7 +569,8 @@ int64_t conv4d_tc_workspace(int64_t cin, const int64_t in[4], int64_t cout, cons
 
 int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void* w, int64_t cout,
                      const int64_t k[4], float* y, int64_t ldy_cf, bool bf16, int S, void* /*workspace*/, int num_sms,
-                     int* dev_status, uint64_t limit_ns, int test_stall, cudaStream_t stream, int* launches)
+                     int* dev_status, uint64_t limit_ns, int test_stall, bool programmatic, cudaStream_t stream,
+                     int* launches)
 {
     (void)num_sms;
     if (S <= 0) S = choose_stack(cin, in, cout, k);
@@ -577,27 +594,31 @@ int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void
     cfg.blockDim = dim3(CT_THREADS, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = programmatic ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, conv4d_tc_pair_kernel, tmX, tmW, p) != cudaSuccess) return GEMM_ERR_CUDA;
     *launches += 1;
     return GEMM_OK;
 }
 
-cudaError_t launch_to_channel_last(const void* src, int64_t B, int64_t C, int64_t V, int64_t Cp, void* dst,
-                                   cudaStream_t stream)
+cudaError_t launch_to_channel_last(const void* x, int64_t C, int64_t V, void* xc, const void* w, int64_t B,
+                                   int64_t T, void* wc, int64_t Cp, cudaStream_t stream)
 {
-    if (B <= 0 || C <= 0 || V <= 0 || Cp < C) return cudaErrorInvalidValue;
-    const int64_t gx = (V + 31) / 32, gy = (Cp + 31) / 32;
-    if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;
-    const dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)(B < 65535 ? B : 65535));
-    to_channel_last_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(src), B, C, V, Cp,
-                                                     static_cast<uint16_t*>(dst));
+    if (C <= 0 || V <= 0 || B <= 0 || T <= 0 || Cp < C || Cp % 16 != 0 ||
+        ((reinterpret_cast<uintptr_t>(xc) | reinterpret_cast<uintptr_t>(wc)) & 15) != 0)
+        return cudaErrorInvalidValue;
+    RelayoutJob jx = {static_cast<const uint16_t*>(x), static_cast<uint16_t*>(xc), 1, C, V, Cp, (V + 255) / 256};
+    RelayoutJob jw = {static_cast<const uint16_t*>(w), static_cast<uint16_t*>(wc), B, C, T, Cp, (T + 255) / 256};
+    const int64_t bx = jx.blocks_per_row * (Cp / 8), bw = jw.blocks_per_row * B * (Cp / 8);
+    if (bx + bw > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    to_channel_last_kernel<<<(unsigned)(bx + bw), 256, 0, stream>>>(jx, jw, bx);
     return cudaGetLastError();
 }
 
