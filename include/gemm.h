@@ -205,7 +205,10 @@ int conv4d_forward(gemm_handle_t h, const float* x, int64_t C_in, const int64_t 
  * consecutive MMAs (16 channels of one window of taps) going round-robin to up to 8
  * partial sums that are added in fp32 round-to-nearest, in order.  Deterministic.
  * Asynchronous on `stream`.  One launch on CTA pairs (tcgen05 cta_group::2), reading x and w
- * straight from the caller's tensors with the Tensor Memory Accelerator; no workspace.
+ * straight from the caller's tensors with the Tensor Memory Accelerator; no workspace.  When
+ * the tiles would fill at most a quarter of the SMs, two pairs (one cluster of four CTAs)
+ * share each tile, each over half of K, and add their partial tiles through distributed
+ * shared memory in a fixed order (deterministic).
  * x, w and y must be 16-byte aligned (GEMM_ERR_ALIGNMENT).
  * GEMM_ERR_INVALID_ARG for bad extents, pointers or dtype (GEMM_BF16 or GEMM_F16 only);
  * GEMM_ERR_UNSUPPORTED unless C_in % 16 == 0, C_out % 16 == 0, S * C_out <= 256,
@@ -287,8 +290,10 @@ typedef enum {
                                    kernel drains its copies and MMAs, frees its tensor memory, returns,
                                    and gemm_get_device_status reports GEMM_ERR_DEVICE_TIMEOUT.  C is not
                                    written.  No fault, trap or unbounded wait is involved. */
-    GEMM_OPT_CONV_STACK = 7     /* tensor-core convolution (conv4d_forward_cl): output positions stacked along
-                                   the MMA's N, 0 choose (default: 2 when in[3] is even and 2*C_out <= 256,
+    GEMM_OPT_CONV_STACK = 7     /* tensor-core convolution (conv4d_forward_cl, conv4d_forward_tc): output
+                                   positions stacked along the MMA's N, 0 choose (default: 4 when that plan,
+                                   with its K split over two CTA pairs per tile, fills between half and all
+                                   of the SMs in one wave; else 2 when in[3] is even and 2*C_out <= 256;
                                    else 1), or 1, 2, 4 */
 } gemm_option_t;
 int gemm_set_option(gemm_handle_t h, int option, int64_t value);

@@ -697,17 +697,12 @@ static int conv4d_forward_cl_impl(gemm_handle_t h, const void* x, int64_t C_in, 
         return GEMM_ERR_ALIGNMENT;
     DeviceGuard g(h->device);
     if (!g.ok()) return GEMM_ERR_CUDA;
-    const int64_t ws = conv4d_tc_workspace(C_in, in_dims, C_out, k_dims, h->opt_conv_stack);
-    if (ws < 0) return GEMM_ERR_UNSUPPORTED;
-    int rc = GEMM_OK;
-    if (ws > 0) {
-        rc = ensure_buffer(reinterpret_cast<void**>(&h->workspace), &h->workspace_bytes, (size_t)ws);
-        if (rc != GEMM_OK) return rc;
-    }
-    glog("conv4d_forward_cl: tensor-core convolution on CTA pairs, workspace %lld bytes (stack option %d)",
-         (long long)ws, h->opt_conv_stack);
+    int rc = conv4d_tc_supported(C_in, in_dims, C_out, k_dims, h->opt_conv_stack, h->num_sms);
+    if (rc != GEMM_OK) return rc;
+    glog("conv4d_forward_cl: tensor-core convolution on CTA pairs, no workspace (stack option %d)",
+         h->opt_conv_stack);
     int n = 0;
-    rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, 0, dtype == GEMM_BF16, h->opt_conv_stack, h->workspace,
+    rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, 0, dtype == GEMM_BF16, h->opt_conv_stack,
                           h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, false,
                           reinterpret_cast<cudaStream_t>(stream), &n);
     h->launches += n;
@@ -737,7 +732,8 @@ static int conv4d_forward_tc_impl(gemm_handle_t h, const void* x, int64_t C_in, 
     const int64_t Cp = (C_in + 15) / 16 * 16;  // channels padded to the MMA's K with zeros
     if (V > (1ll << 40) || T > (1ll << 40) || (double)V * Cp >= 9.0e15 || (double)C_out * T * Cp >= 9.0e15)
         return GEMM_ERR_UNSUPPORTED;
-    if (conv4d_tc_workspace(Cp, in_dims, C_out, k_dims, h->opt_conv_stack) < 0) return GEMM_ERR_UNSUPPORTED;
+    if (conv4d_tc_supported(Cp, in_dims, C_out, k_dims, h->opt_conv_stack, h->num_sms) != GEMM_OK)
+        return GEMM_ERR_UNSUPPORTED;
     DeviceGuard g(h->device);
     if (!g.ok()) return GEMM_ERR_CUDA;
     // channel-last copies of x and w in the workspace, each on a 256-byte boundary
@@ -755,7 +751,7 @@ static int conv4d_forward_tc_impl(gemm_handle_t h, const void* x, int64_t C_in, 
     h->launches += 1;
     int n = 0;
     rc = launch_conv4d_tc(xc, Cp, in_dims, wc, C_out, k_dims, y, ldy, dtype == GEMM_BF16, h->opt_conv_stack,
-                          h->workspace, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, true, s, &n);
+                          h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, true, s, &n);
     h->launches += n;
     return rc;
 }

@@ -45,6 +45,14 @@
 //     accumulators; the tensor core's fp32 accumulator rounds toward zero, so shorter sums
 //     per accumulator keep the error small; the epilogue adds them in fp32
 //     round-to-nearest, in order.  Deterministic.
+// K split.  With tiles for at most a quarter of the SMs, a tile is a cluster of four CTAs:
+// two pairs, each over half of the stage sequence.  Each CTA's epilogue leaves its partial
+// part (128 rows x N fp32) in its own shared memory (the operand ring, idle by then); after
+// a cluster barrier each pair stores half of the columns, adding slot 0's part and slot 1's
+// in that order, the other slot's read through distributed shared memory; a second cluster
+// barrier keeps every part alive until it has been read.  Both barriers are reached by every
+// thread on every path.  At 16^4 x 16 -> 32 channels, 5^4 filter this lets four positions
+// stack along N (N = 128: MMAs at the full rate) on 144 CTAs: 35.5 us against 37.6 us.
 // Every mbarrier wait is bounded (wall clock); on expiry the CTA records an error in the
 // status word, waits (bounded) for its own copies and MMAs in flight, frees its TMEM and
 // returns.
@@ -66,6 +74,7 @@ constexpr int CT_MAX_ACC = 8;       // TMEM accumulators (round-robin)
 constexpr int CT_TMEM_COLS = 512;
 constexpr int CT_SMEM_BUDGET = 200 * 1024;  // pipeline stages
 constexpr int CT_MAX_STAGES = 8;
+constexpr int CT_MAX_KS = 2;        // pairs per tile (K split over the stage sequence)
 
 struct ConvTcParams {
     int cin, cout, S;
@@ -86,7 +95,10 @@ struct ConvTcParams {
     int num_stages;     // R0 * R1 * r2_groups * k_groups
     int issuers;        // MMA-issuing threads (1 .. CT_ISSUERS_MAX)
     int nacc;           // TMEM accumulators (issuer i owns i, i + issuers, ...)
-    uint32_t acc_used;  // bit a: accumulator a receives at least one MMA
+    int ks;             // pairs per tile (1 or 2): pair j of a tile's cluster runs stages
+                        // [j n / ks, (j + 1) n / ks) and the pairs add their parts through
+                        // distributed shared memory
+    uint32_t acc_used[CT_MAX_KS];  // per K slot, bit a: accumulator a receives at least one MMA
     int tmem_cols;
     uint32_t idesc;
     float* y;
@@ -129,12 +141,16 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const uint32_t rank = cluster_ctarank();  // CTA within the pair
-
-    // this pair: output slab p0, positions u0 .. u0 + 256 S - 1; this CTA: its 128 rows
-    const int pair = blockIdx.x / 2;
-    const int p0 = pair / p.tiles_per_p0;
-    const int u0 = (pair % p.tiles_per_p0) * 2 * CT_G * p.S;
+    // a cluster is one tile: ks pairs of CTAs, pair j (cluster ranks 2j, 2j + 1) for K slot j
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t rank = crank & 1u;          // CTA within the pair
+    const uint32_t leader = crank & ~1u;       // the pair's even CTA (cluster rank)
+    const uint16_t pair_mask = (uint16_t)(0x3u << leader);
+    const int tile = blockIdx.x / (2 * p.ks), kslot = (int)(crank >> 1);
+    const int p0 = tile / p.tiles_per_p0;
+    const int u0 = (tile % p.tiles_per_p0) * 2 * CT_G * p.S;
+    const int st_begin = (int)((int64_t)kslot * p.num_stages / p.ks);
+    const int st_end = (int)((int64_t)(kslot + 1) * p.num_stages / p.ks);
     const int q_cta = u0 / p.S + (int)rank * CT_G;  // first input row (u / S) of this CTA's tile rows
     const int N = p.S * p.cout;
     const int half = p.cout / 2;
@@ -162,6 +178,82 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     const uint32_t tmem_base = *tmem_holder;
     bool aborted = false;
 
+    // epilogue (warps CT_ISSUERS_MAX + 1 ..): thread = tile row g of this CTA, TMEM lane quarter
+    // `quarter`; columns in chunks of 32 (a last chunk of 16 when N % 32 == 16), or of 16 for
+    // the K split.  The accumulators' parts of a chunk are added in order, then stored as
+    // groups of 8 columns.  Column c = h (S C_out/2) + t' (C_out/2) + o_low is output channel
+    // h C_out/2 + o_low at position ug + S - 1 - t'
+    const int quarter = warp & 3;
+    const int ug = u0 + ((int)rank * CT_G + quarter * 32 + lane) * p.S;  // this row's first position
+    const int plane = p.I[2] * p.I[3];
+    const uint32_t used = p.acc_used[kslot];
+    float* const my_part = reinterpret_cast<float*>(smem) + quarter * N * 32;  // K split: [column][lane]
+    bool epi_ok = false;
+    // the accumulators that received MMAs, added in order; 16-column chunks load four
+    // accumulators per wait (the 32-column form has no registers to spare for that)
+    auto chunk_sum = [&](int c0, int w, auto& acc) {
+        constexpr int CW = sizeof(acc) / sizeof(acc[0]);
+        constexpr int BATCH = CW == 16 ? 4 : 1;
+#pragma unroll
+        for (int i = 0; i < CW; ++i) acc[i] = 0.f;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0;
+        if (CW == 32 && w == 16) {  // a last chunk of 16 columns, one accumulator at a time
+            for (int a = 0; a < p.nacc; ++a) {
+                if (!((used >> a) & 1)) continue;
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * N), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __uint_as_float(v[i]));
+            }
+            return;
+        }
+        for (int a0 = 0; a0 < p.nacc; a0 += BATCH) {
+            uint32_t v[BATCH][CW];
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const int a = a0 + b;
+                if (a >= p.nacc || !((used >> a) & 1)) continue;
+                if constexpr (CW == 32)
+                    tmem_ld_32x32b_x32(lane_base + (uint32_t)(a * N), v[b]);
+                else
+                    tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * N), v[b]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const int a = a0 + b;
+                if (a >= p.nacc || !((used >> a) & 1)) continue;
+#pragma unroll
+                for (int i = 0; i < CW; ++i) acc[i] = __fadd_rn(acc[i], __uint_as_float(v[b][i]));
+            }
+        }
+    };
+    auto chunk_store = [&](int c0, int w, const auto& acc) {
+        constexpr int CW = sizeof(acc) / sizeof(acc[0]);
+#pragma unroll
+        for (int j = 0; j < CW; j += 8) {
+            if (j >= w) break;
+            const int c = c0 + j;
+            const int hh = c / (N / 2), cr = c - hh * (N / 2);
+            const int tb = cr / half, o = hh * half + (cr - tb * half);
+            const int u = ug + p.S - 1 - tb;
+            const int p1 = u / plane, rem = u - p1 * plane;
+            const int p2 = rem / p.I[3], p3 = rem - p2 * p.I[3];
+            if (p1 < p.P[1] && p2 < p.P[2] && p3 < p.P[3] && in_range(p0, p.P[0]) && in_range(o + 7, p.cout)) {
+                const int64_t pos = (((int64_t)p0 * p.P[1] + p1) * p.P[2] + p2) * p.P[3] + p3;
+                if (p.ldy_cf == 0) {
+                    float* yrow = p.y + pos * p.cout + o;
+                    *reinterpret_cast<float4*>(yrow) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                    *reinterpret_cast<float4*>(yrow + 4) = make_float4(acc[j + 4], acc[j + 5], acc[j + 6], acc[j + 7]);
+                } else {
+                    float* ycol = p.y + (int64_t)o * p.ldy_cf + pos;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ycol[(int64_t)e * p.ldy_cf] = acc[j + e];
+                }
+            }
+        }
+    };
     if (warp == 0) {
         // ---------------------------------------------------------------- producer (both CTAs)
         if (lane == 0) {
@@ -169,16 +261,21 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
             // and visible before the first copy (a no-op after an ordinary launch)
             asm volatile("griddepcontrol.wait;" ::: "memory");
             uint32_t issued_mask = 0, last_parity = 0;
-            int slot = 0, r0 = 0, r1 = 0, grp = 0, kg = 0;
+            // stage st = ((r0 R1 + r1) r2_groups + grp) k_groups + kg
+            int kg = st_begin % p.k_groups, t = st_begin / p.k_groups;
+            int grp = t % p.r2_groups;
+            t /= p.r2_groups;
+            int r1 = t % p.R[1], r0 = t / p.R[1];
+            int slot = 0;
             uint32_t ph = 0;
-            for (int st = 0; st < p.num_stages; ++st) {
+            for (int st = st_begin; st < st_end; ++st) {
                 if (!mbar_wait_cluster(smem_u32(&empty_bar[slot]), ph ^ 1, p.limit_ns, abort_flag)) {
                     ct_record_error(p.status, kDevTimeoutProducer, abort_flag);
                     aborted = true;
                     break;
                 }
                 const uint32_t fb_local = smem_u32(&full_bar[slot]);
-                const uint32_t fb_even = mapa_shared(fb_local, 0);
+                const uint32_t fb_even = mapa_shared(fb_local, leader);
                 if (rank == 0) mbar_arrive_expect_tx(fb_local, 2u * (uint32_t)p.tx_bytes);
                 const uint32_t st_base = smem_u32(smem + slot * p.stage_bytes);
                 const int r2f = grp * p.g2;
@@ -242,9 +339,9 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
             const uint32_t my_acc = (uint32_t)(p.nacc / T);
             const int s_log2 = p.S == 4 ? 2 : p.S == 2 ? 1 : 0;
             uint32_t mma = 0, acc_j = 0;
-            int slot = 0, grp = 0;
+            int slot = 0, grp = (st_begin / p.k_groups) % p.r2_groups;
             uint32_t ph = 0;
-            for (int st = 0; st < p.num_stages; ++st) {
+            for (int st = st_begin; st < st_end; ++st) {
                 if (!mbar_wait_cluster(smem_u32(&full_bar[slot]), ph, p.limit_ns, abort_flag)) {
                     ct_record_error(p.status, kDevTimeoutMma, abort_flag);
                     ok = false;
@@ -283,17 +380,17 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
                         }
                     }
                 }
-                umma_commit_mask(smem_u32(&empty_bar[slot]), 0x3);  // stage free in both CTAs
+                umma_commit_mask(smem_u32(&empty_bar[slot]), pair_mask);  // stage free in both CTAs
                 if (++slot == SA) {
                     slot = 0;
                     ph ^= 1;
                 }
                 if ((st + 1) % p.k_groups == 0 && ++grp == p.r2_groups) grp = 0;
             }
-            if (ok) umma_commit_mask(smem_u32(done_bar), 0x3);
+            if (ok) umma_commit_mask(smem_u32(done_bar), pair_mask);
             else aborted = true;
             // no MMA of this pair may still be running when TMEM and shared memory are released
-            umma_commit_mask(smem_u32(drain_bar), 0x3);
+            umma_commit_mask(smem_u32(drain_bar), pair_mask);
         }
         if (lane == 0 && warp - 1 < p.issuers) {
             // (the odd CTA's issuer warps wait here the whole main loop: sleep between polls)
@@ -305,7 +402,6 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
         __syncwarp();
     } else {
         // ---------------------------------------------------------------- epilogue (both CTAs)
-        const int quarter = warp & 3;  // TMEM lane quarter this warp may access
         bool ok = true;
         if (p.test_stall) {
             // test hook: a wait nothing will satisfy runs out and takes the abort path
@@ -322,58 +418,48 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
         if (!ok) aborted = true;
         if (ok) {
             tc_fence_after();
-            const int g = quarter * 32 + lane;          // tile row of this thread
-            const int ug = u0 + ((int)rank * CT_G + g) * p.S;  // its first position
-            const int plane = p.I[2] * p.I[3];
-            // columns in chunks of 32 (a last chunk of 16 when N % 32 == 16): the accumulators'
-            // parts of a chunk are added in order, then stored as groups of 8 columns.  Column
-            // c = h (S C_out/2) + t' (C_out/2) + o_low is output channel h C_out/2 + o_low at
-            // position ug + S - 1 - t'
-            for (int c0 = 0; c0 < N; c0 += 32) {
-                const int w = N - c0 >= 32 ? 32 : 16;
-                float acc[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-                for (int a = 0; a < p.nacc; ++a) {  // the accumulators that received MMAs, in order
-                    if (!((p.acc_used >> a) & 1)) continue;
-                    const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * N + c0);
-                    if (w == 32) {
-                        uint32_t v[32];
-                        tmem_ld_32x32b_x32(taddr, v);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[i] = __fadd_rn(acc[i], __uint_as_float(v[i]));
-                    } else {
-                        uint32_t v[16];
-                        tmem_ld_32x32b_x16(taddr, v);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __uint_as_float(v[i]));
-                    }
+            epi_ok = true;
+            if (p.ks == 1) {
+                for (int c0 = 0; c0 < N; c0 += 32) {
+                    const int w = N - c0 >= 32 ? 32 : 16;
+                    float acc[32];
+                    chunk_sum(c0, w, acc);
+                    chunk_store(c0, w, acc);
                 }
+            } else {
+                // K split: this warp's partial part (32 rows x N columns) goes to this CTA's
+                // shared memory (the operand ring, idle once the MMAs are done), laid out
+                // [column][lane] so that a warp's accesses are conflict-free 128-byte rows
+                for (int c0 = 0; c0 < N; c0 += 16) {
+                    float acc[16];
+                    chunk_sum(c0, 16, acc);
 #pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    if (j >= w) break;
-                    const int c = c0 + j;
-                    const int hh = c / (N / 2), cr = c - hh * (N / 2);
-                    const int tb = cr / half, o = hh * half + (cr - tb * half);
-                    const int u = ug + p.S - 1 - tb;
-                    const int p1 = u / plane, rem = u - p1 * plane;
-                    const int p2 = rem / p.I[3], p3 = rem - p2 * p.I[3];
-                    if (p1 < p.P[1] && p2 < p.P[2] && p3 < p.P[3] && in_range(p0, p.P[0]) && in_range(o + 7, p.cout)) {
-                        const int64_t pos = (((int64_t)p0 * p.P[1] + p1) * p.P[2] + p2) * p.P[3] + p3;
-                        if (p.ldy_cf == 0) {
-                            float* yrow = p.y + pos * p.cout + o;
-                            *reinterpret_cast<float4*>(yrow) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                            *reinterpret_cast<float4*>(yrow + 4) =
-                                make_float4(acc[j + 4], acc[j + 5], acc[j + 6], acc[j + 7]);
-                        } else {
-                            float* ycol = p.y + (int64_t)o * p.ldy_cf + pos;
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) ycol[(int64_t)e * p.ldy_cf] = acc[j + e];
-                        }
-                    }
+                    for (int i = 0; i < 16; ++i) my_part[(c0 + i) * 32 + lane] = acc[i];
                 }
+            }
+        }
+    }
+
+    if (p.ks == 2) {
+        // every CTA's part is in its shared memory (all threads of the cluster arrive, on every
+        // path); then each slot's CTA adds the two parts of its rows for half of the columns,
+        // slot 0's part + slot 1's part, reading the other slot's through distributed shared
+        // memory, and stores y
+        cluster_sync_all();
+        if (epi_ok) {
+            const uint32_t peer = crank ^ 2u;  // the same rows in the other slot's pair
+            const int c_lo = kslot * (N / 2);
+            for (int c0 = c_lo; c0 < c_lo + N / 2; c0 += 16) {
+                float other[16], acc[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    other[i] = ld_shared_cluster_f32(mapa_shared(smem_u32(my_part + (c0 + i) * 32 + lane), peer));
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float own = my_part[(c0 + i) * 32 + lane];
+                    acc[i] = kslot == 0 ? __fadd_rn(own, other[i]) : __fadd_rn(other[i], own);
+                }
+                chunk_store(c0, 16, acc);
             }
         }
     }
@@ -461,8 +547,25 @@ bool encode_conv_maps(CUtensorMap* tmX, CUtensorMap* tmW, const void* x, const v
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Stages in [a, b) whose filter-row group is gg; stage st has group (st / kg) % r2g.
+int64_t stages_of_group(int64_t a, int64_t b, int64_t kg, int64_t r2g, int64_t gg)
+{
+    if (b <= a) return 0;
+    auto blocks_below = [&](int64_t j) { return j / r2g + ((j % r2g) > gg ? 1 : 0); };  // j' < j with j' % r2g == gg
+    const int64_t ja = a / kg, jb = (b - 1) / kg;  // first and last block of kg stages touched
+    if (ja == jb) return (ja % r2g == gg) ? b - a : 0;
+    int64_t n = 0;
+    if (ja % r2g == gg) n += (ja + 1) * kg - a;
+    if (jb % r2g == gg) n += b - jb * kg;
+    n += (blocks_below(jb) - blocks_below(ja + 1)) * kg;
+    return n;
+}
+
 // Tiling and pipeline of the convolution for stack S (GEMM_OK or GEMM_ERR_UNSUPPORTED).
-int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S, ConvTcParams* out)
+// With tiles for fewer than half the SMs' pairs, the stage sequence of each tile is split
+// over ks pairs (K split), so that the pairs fill the SMs.
+int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S, int num_sms,
+                   ConvTcParams* out)
 {
     ConvTcParams p = {};
     if (cin % 16 || cout % 16 || S < 1 || in[3] % S || S * cout > 256) return GEMM_ERR_UNSUPPORTED;
@@ -529,18 +632,33 @@ int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t
     p.issuers = nacc < CT_ISSUERS_MAX ? nacc : CT_ISSUERS_MAX;
     nacc -= nacc % p.issuers;
     p.nacc = nacc;
-    // accumulator i + issuers j is written iff issuer i issues more than j MMAs over the call;
-    // issuer i takes MMAs [i n / issuers, (i + 1) n / issuers) of every stage of n MMAs
-    p.acc_used = 0;
-    for (int a = 0; a < nacc; ++a) {
-        const int issuer = a % p.issuers, j = a / p.issuers;
-        int64_t mine = 0;
-        for (int grp = 0; grp < p.r2_groups; ++grp) {
-            const int g = (p.R[2] - grp * p.g2) < p.g2 ? p.R[2] - grp * p.g2 : p.g2;
-            const int64_t n = (int64_t)g * windows * p.kq;
-            mine += (issuer + 1) * n / p.issuers - issuer * n / p.issuers;
+    // K split: two pairs per tile (a cluster of four CTAs) when one pair per tile would leave
+    // more than half the SMs idle, N is a multiple of 32 (each slot stores half the columns in
+    // 16-column chunks), there are at least two stages, and the partial parts (128 rows x N
+    // fp32 per CTA) fit in the operand ring
+    const int64_t tiles = (int64_t)p.tiles_per_p0 * p.P[0];
+    p.ks = (num_sms > 0 && 4 * tiles <= num_sms && N % 32 == 0 && p.num_stages >= 2 &&
+            (int64_t)p.nstages_ring * p.stage_bytes >= (int64_t)CT_G * N * 4)
+               ? 2
+               : 1;
+    if (tiles * p.ks * 2 > 0x7fffffff) return GEMM_ERR_UNSUPPORTED;
+    // accumulator i + issuers j of slot s is written iff issuer i issues more than j MMAs
+    // in the slot's stages; issuer i takes MMAs [i n / issuers, (i + 1) n / issuers) of
+    // every stage of n MMAs, and n depends on the stage's filter-row group
+    for (int sl = 0; sl < CT_MAX_KS; ++sl) p.acc_used[sl] = 0;
+    for (int sl = 0; sl < p.ks; ++sl) {
+        const int64_t a0 = (int64_t)sl * nst / p.ks, b0 = (int64_t)(sl + 1) * nst / p.ks;
+        for (int a = 0; a < nacc; ++a) {
+            const int issuer = a % p.issuers, j = a / p.issuers;
+            int64_t mine = 0;
+            for (int grp = 0; grp < p.r2_groups; ++grp) {
+                const int g = (p.R[2] - grp * p.g2) < p.g2 ? p.R[2] - grp * p.g2 : p.g2;
+                const int64_t n = (int64_t)g * windows * p.kq;
+                mine += stages_of_group(a0, b0, p.k_groups, p.r2_groups, grp) *
+                        ((issuer + 1) * n / p.issuers - issuer * n / p.issuers);
+            }
+            if (mine > j) p.acc_used[sl] |= 1u << a;
         }
-        if (mine * k[0] * k[1] * p.k_groups > j) p.acc_used |= 1u << a;
     }
     p.tmem_cols = 32;
     while (p.tmem_cols < nacc * N) p.tmem_cols *= 2;
@@ -548,35 +666,41 @@ int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t
     return GEMM_OK;
 }
 
-// Positions stacked along N: 2 when the shape allows it, else 1.
-int choose_stack(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4])
+// Positions stacked along N.  Four (N = 4 C_out, MMAs at the full rate from N = 128 on)
+// when that plan, with its K split, fits the SMs in one wave and fills at least half of
+// them: at 16^4 x 16 -> 32 channels, 5^4 filter, 35.5 us against 37.6 us for two positions
+// without a split, although the stacked zero blocks grow from 1/6 to 3/8 of the products.
+// Else two when the shape allows it, else one.
+int choose_stack(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int num_sms)
 {
     ConvTcParams p;
+    if (plan_conv4d_tc(cin, in, cout, k, 4, num_sms, &p) == GEMM_OK) {
+        const int64_t ctas = (int64_t)2 * p.ks * p.tiles_per_p0 * p.P[0];
+        if (p.ks == 2 && ctas <= num_sms && 2 * ctas >= num_sms) return 4;
+    }
     for (int S : {2, 1})
-        if (plan_conv4d_tc(cin, in, cout, k, S, &p) == GEMM_OK) return S;
+        if (plan_conv4d_tc(cin, in, cout, k, S, num_sms, &p) == GEMM_OK) return S;
     return 0;
 }
 
 }  // namespace
 
-int64_t conv4d_tc_workspace(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S)
+int conv4d_tc_supported(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S, int num_sms)
 {
     ConvTcParams p;
-    if (S <= 0) S = choose_stack(cin, in, cout, k);
-    if (S <= 0 || plan_conv4d_tc(cin, in, cout, k, S, &p) != GEMM_OK) return -1;
-    return 0;  // the operands are read straight from the caller's tensors
+    if (S <= 0) S = choose_stack(cin, in, cout, k, num_sms);
+    if (S <= 0 || plan_conv4d_tc(cin, in, cout, k, S, num_sms, &p) != GEMM_OK) return GEMM_ERR_UNSUPPORTED;
+    return GEMM_OK;  // the operands are read straight from the caller's tensors: no workspace
 }
 
 int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void* w, int64_t cout,
-                     const int64_t k[4], float* y, int64_t ldy_cf, bool bf16, int S, void* /*workspace*/, int num_sms,
-                     int* dev_status, uint64_t limit_ns, int test_stall, bool programmatic, cudaStream_t stream,
-                     int* launches)
+                     const int64_t k[4], float* y, int64_t ldy_cf, bool bf16, int S, int num_sms, int* dev_status,
+                     uint64_t limit_ns, int test_stall, bool programmatic, cudaStream_t stream, int* launches)
 {
-    (void)num_sms;
-    if (S <= 0) S = choose_stack(cin, in, cout, k);
+    if (S <= 0) S = choose_stack(cin, in, cout, k, num_sms);
     if (S <= 0) return GEMM_ERR_UNSUPPORTED;
     ConvTcParams p;
-    const int rc = plan_conv4d_tc(cin, in, cout, k, S, &p);
+    const int rc = plan_conv4d_tc(cin, in, cout, k, S, num_sms, &p);
     if (rc != GEMM_OK) return rc;
     p.idesc = conv_idesc(bf16, S * p.cout);
     p.y = y;
@@ -590,13 +714,13 @@ int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void
     if (cudaFuncSetAttribute(conv4d_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * p.tiles_per_p0 * p.P[0]), 1, 1);
+    cfg.gridDim = dim3((unsigned)(2 * p.ks * p.tiles_per_p0 * p.P[0]), 1, 1);
     cfg.blockDim = dim3(CT_THREADS, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = 2 * p.ks;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -106,22 +106,6 @@ __device__ __forceinline__ void pt_tile_coord(const PtParams& p, int t, int& mt,
     nt = (t % width) / gsize;
 }
 
-// Count one finished slice on a counter whose upper half holds the launch's tag: a count
-// left by another launch (or an aborted one) restarts at 1.  Returns the arrival number
-// (1 = first), or 0 if the counter kept changing under us (reported as an error).
-__device__ __forceinline__ int pt_slice_arrive(unsigned long long* counter, uint32_t seq)
-{
-    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(counter);
-    for (int i = 0; i < (1 << 20); ++i) {
-        const unsigned long long nxt =
-            ((uint32_t)(cur >> 32) == seq) ? cur + 1 : (((unsigned long long)seq << 32) | 1ull);
-        const unsigned long long prev = atomicCAS(counter, cur, nxt);
-        if (prev == cur) return (int)(uint32_t)nxt;
-        cur = prev;
-    }
-    return 0;
-}
-
 __device__ __forceinline__ void pt_fail(int* status, int code, volatile int* abort_flag)
 {
     atomicCAS(status, 0, code);
@@ -180,7 +164,7 @@ ffma_persistent_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         if (first) {
             p_item = blockIdx.x;
         } else {
-            const int n = pt_slice_arrive(p.cnt + (p.num_tiles - p.split_first), p.seq);
+            const int n = tagged_arrive(p.cnt + (p.num_tiles - p.split_first), p.seq);
             p_item = n > 0 ? (int)gridDim.x + n - 1 : p.num_items;
             if (n == 0) pt_fail(p.status, kDevTimeoutProducer, abort_flag);
         }
@@ -329,7 +313,7 @@ ffma_persistent_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             __threadfence();
             __syncthreads();
             if (tid == 0) {
-                const int n = ws_ok ? pt_slice_arrive(p.cnt + st, p.seq) : 0;
+                const int n = ws_ok ? tagged_arrive(p.cnt + st, p.seq) : 0;
                 if (n == 0) pt_fail(p.status, kDevTimeoutEpilogue, abort_flag);
                 *bcast = n;
             }

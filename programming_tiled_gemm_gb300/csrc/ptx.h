@@ -116,6 +116,14 @@ __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr)
     return v;
 }
 
+// 4 bytes from a cluster shared-memory address (another CTA's shared memory).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Barrier over every thread of every CTA of the cluster (warps converged); release /
 // acquire at cluster scope, so shared-memory writes before it are visible to all CTAs'
 // reads after it.
@@ -454,6 +462,25 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap
         " [%0], [%1, {%3, %4, %5, %6}], [%2];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
+}
+
+
+// Count one arrival on a 64-bit counter whose upper half holds a launch tag: a count left
+// by another launch (or by one that stopped early) restarts at 1.  Returns the arrival
+// number in this launch (1 = first), or 0 if the counter kept changing under us (the
+// caller reports an error).  Used where the last of several CTAs or warps to finish a
+// piece of work takes over the rest of it, so that nothing waits for anyone.
+__device__ __forceinline__ int tagged_arrive(unsigned long long* counter, uint32_t seq)
+{
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(counter);
+    for (int i = 0; i < (1 << 20); ++i) {
+        const unsigned long long nxt =
+            ((uint32_t)(cur >> 32) == seq) ? cur + 1 : (((unsigned long long)seq << 32) | 1ull);
+        const unsigned long long prev = atomicCAS(counter, cur, nxt);
+        if (prev == cur) return (int)(uint32_t)nxt;
+        cur = prev;
+    }
+    return 0;
 }
 
 }  // namespace gemm_gb300

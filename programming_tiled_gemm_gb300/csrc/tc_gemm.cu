@@ -266,22 +266,6 @@ __device__ __forceinline__ PairItem pair_item(const TcParams& p, int it)
 constexpr int MAX_REM_SPLIT = 4;
 constexpr int REM_PART_FLOATS = 32 * EPI_COLS;  // one epilogue warp's 32 rows x 128 columns
 
-// Count one finished K slice of a tile part; returns the number of slices finished so far
-// in this launch (0 if the update kept failing).  The counter's upper half holds the launch
-// tag: a count left by another launch (one that stopped early) restarts at 1.
-__device__ __forceinline__ int slice_arrive(unsigned long long* counter, uint32_t seq)
-{
-    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(counter);
-    for (int i = 0; i < (1 << 20); ++i) {
-        const unsigned long long nxt =
-            ((uint32_t)(cur >> 32) == seq) ? cur + 1 : (((unsigned long long)seq << 32) | 1ull);
-        const unsigned long long prev = atomicCAS(counter, cur, nxt);
-        if (prev == cur) return (int)(uint32_t)nxt;
-        cur = prev;
-    }
-    return 0;
-}
-
 // Last-wave split, one epilogue warp's part (32 rows x 128 columns, thread = row) of K
 // slice `sl` of split tile j: publish it, count it, and if it is the part's last slice to
 // finish, replace `tot` by the sum of all slices in slice order (true: store C).  Nothing
@@ -302,7 +286,7 @@ __device__ __forceinline__ bool rem_slice_combine(const TcParams& p, float (&tot
     __syncwarp();
     int n = 0;
     if (lane == 0) {
-        n = slice_arrive(p.rem_cnt + ((int64_t)j * 2 + cta) * EPI_WARPS + w, p.rem_seq);
+        n = tagged_arrive(p.rem_cnt + ((int64_t)j * 2 + cta) * EPI_WARPS + w, p.rem_seq);
         if (n == 0) record_error(status, kDevTimeoutEpilogue, abort_flag);
     }
     n = __shfl_sync(0xffffffffu, n, 0);
@@ -889,7 +873,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (!in_range(part, (int64_t)(p.num_tiles - p.rem_first) * 2 * EPI_WARPS)) continue;
                 int n = 0;
                 if (lane == 0) {
-                    n = slice_arrive(p.rem_cnt + part, p.rem_seq);
+                    n = tagged_arrive(p.rem_cnt + part, p.rem_seq);
                     if (n == 0) record_error(p.status, kDevTimeoutEpilogue, abort_flag);
                 }
                 n = __shfl_sync(0xffffffffu, n, 0);
