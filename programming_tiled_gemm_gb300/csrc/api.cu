@@ -6,16 +6,12 @@
 // multiplication" (set up device buffers once, pass (m, n, k, a, b, c) to the kernel,
 // enqueue it on a queue, wait on an event): here a handle is created once, gemm_run
 // enqueues on the caller's CUDA stream, and the caller synchronises as it wishes.
+#include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
-
-#include <cstdarg>
-#include <cstdio>
-#include <cstdlib>
-#include <cstring>
 
 #include "internal.h"
 

@@ -562,8 +562,8 @@ int64_t stages_of_group(int64_t a, int64_t b, int64_t kg, int64_t r2g, int64_t g
 }
 
 // Tiling and pipeline of the convolution for stack S (GEMM_OK or GEMM_ERR_UNSUPPORTED).
-// With tiles for fewer than half the SMs' pairs, the stage sequence of each tile is split
-// over ks pairs (K split), so that the pairs fill the SMs.
+// With tiles for at most a quarter of the SMs, the stage sequence of each tile is split
+// over two pairs (K split, a cluster of four CTAs), so that the pairs fill the SMs.
 int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S, int num_sms,
                    ConvTcParams* out)
 {
