@@ -290,11 +290,16 @@ typedef enum {
                                    kernel drains its copies and MMAs, frees its tensor memory, returns,
                                    and gemm_get_device_status reports GEMM_ERR_DEVICE_TIMEOUT.  C is not
                                    written.  No fault, trap or unbounded wait is involved. */
-    GEMM_OPT_CONV_STACK = 7     /* tensor-core convolution (conv4d_forward_cl, conv4d_forward_tc): output
+    GEMM_OPT_CONV_STACK = 7,    /* tensor-core convolution (conv4d_forward_cl, conv4d_forward_tc): output
                                    positions stacked along the MMA's N, 0 choose (default: 4 when that plan,
                                    with its K split over two CTA pairs per tile, fills between half and all
                                    of the SMs in one wave; else 2 when in[3] is even and 2*C_out <= 256;
                                    else 1), or 1, 2, 4 */
+    GEMM_OPT_CONV_SPLIT = 8     /* tensor-core convolution: K split over CTA pairs, 0 choose (default: two
+                                   pairs per tile when the tiles would fill at most a quarter of the SMs),
+                                   1 one pair per tile, 2 two pairs per tile (GEMM_ERR_UNSUPPORTED from the
+                                   convolution when S*C_out is not a multiple of 32 or there is a single
+                                   pipeline stage) */
 } gemm_option_t;
 int gemm_set_option(gemm_handle_t h, int option, int64_t value);
 

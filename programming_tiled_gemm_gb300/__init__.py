@@ -27,6 +27,7 @@ GEMM_ERR_DEVICE_BOUNDS = -6
 GEMM_OPT_F32_KERNEL, GEMM_OPT_SPLIT_K, GEMM_OPT_WAIT_LIMIT_US, GEMM_OPT_TC_CHUNK, GEMM_OPT_TC_PAIR = 1, 2, 3, 4, 5
 GEMM_OPT_TEST_STALL = 6
 GEMM_OPT_CONV_STACK = 7
+GEMM_OPT_CONV_SPLIT = 8
 
 # Every symbol include/gemm.h declares (the ABI test checks the library exports them).
 EXPORTS = ["gemm_create", "gemm_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host", "gemm_run_host_batch",

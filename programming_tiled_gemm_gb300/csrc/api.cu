@@ -91,6 +91,7 @@ struct gemm_ctx {
     int opt_tc_pair = 0;   // tensor-core tile: 0 choose, 1 single CTA, 2 CTA pair
     int opt_test_stall = 0;  // test hook: kernels with bounded waits let one wait run out
     int opt_conv_stack = 0;  // tensor-core convolution: output positions stacked along N (0 = choose)
+    int opt_conv_split = 0;  // tensor-core convolution: 0 choose, 1 one CTA pair per tile, 2 two pairs
     uint64_t wait_limit_ns = 2000000000ull;
     int64_t launches = 0;  // kernels launched through this handle
     // gemm_run_host pipeline: copy-in and copy-out streams and their events
@@ -304,6 +305,10 @@ static int gemm_set_option_impl(gemm_handle_t h, int option, int64_t value)
     case GEMM_OPT_CONV_STACK:
         if (value != 0 && value != 1 && value != 2 && value != 4) return GEMM_ERR_INVALID_ARG;
         h->opt_conv_stack = (int)value;
+        return GEMM_OK;
+    case GEMM_OPT_CONV_SPLIT:
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+        h->opt_conv_split = (int)value;
         return GEMM_OK;
     case GEMM_OPT_TEST_STALL:
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
@@ -693,13 +698,13 @@ static int conv4d_forward_cl_impl(gemm_handle_t h, const void* x, int64_t C_in, 
         return GEMM_ERR_ALIGNMENT;
     DeviceGuard g(h->device);
     if (!g.ok()) return GEMM_ERR_CUDA;
-    int rc = conv4d_tc_supported(C_in, in_dims, C_out, k_dims, h->opt_conv_stack, h->num_sms);
+    int rc = conv4d_tc_supported(C_in, in_dims, C_out, k_dims, h->opt_conv_stack, h->opt_conv_split, h->num_sms);
     if (rc != GEMM_OK) return rc;
-    glog("conv4d_forward_cl: tensor-core convolution on CTA pairs, no workspace (stack option %d)",
-         h->opt_conv_stack);
+    glog("conv4d_forward_cl: tensor-core convolution on CTA pairs, no workspace (stack option %d, split option %d)",
+         h->opt_conv_stack, h->opt_conv_split);
     int n = 0;
     rc = launch_conv4d_tc(x, C_in, in_dims, w, C_out, k_dims, y, 0, dtype == GEMM_BF16, h->opt_conv_stack,
-                          h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, false,
+                          h->opt_conv_split, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, false,
                           reinterpret_cast<cudaStream_t>(stream), &n);
     h->launches += n;
     return rc;
@@ -728,7 +733,7 @@ static int conv4d_forward_tc_impl(gemm_handle_t h, const void* x, int64_t C_in, 
     const int64_t Cp = (C_in + 15) / 16 * 16;  // channels padded to the MMA's K with zeros
     if (V > (1ll << 40) || T > (1ll << 40) || (double)V * Cp >= 9.0e15 || (double)C_out * T * Cp >= 9.0e15)
         return GEMM_ERR_UNSUPPORTED;
-    if (conv4d_tc_supported(Cp, in_dims, C_out, k_dims, h->opt_conv_stack, h->num_sms) != GEMM_OK)
+    if (conv4d_tc_supported(Cp, in_dims, C_out, k_dims, h->opt_conv_stack, h->opt_conv_split, h->num_sms) != GEMM_OK)
         return GEMM_ERR_UNSUPPORTED;
     DeviceGuard g(h->device);
     if (!g.ok()) return GEMM_ERR_CUDA;
@@ -747,7 +752,7 @@ static int conv4d_forward_tc_impl(gemm_handle_t h, const void* x, int64_t C_in, 
     h->launches += 1;
     int n = 0;
     rc = launch_conv4d_tc(xc, Cp, in_dims, wc, C_out, k_dims, y, ldy, dtype == GEMM_BF16, h->opt_conv_stack,
-                          h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, true, s, &n);
+                          h->opt_conv_split, h->num_sms, h->d_status, h->wait_limit_ns, h->opt_test_stall, true, s, &n);
     h->launches += n;
     return rc;
 }

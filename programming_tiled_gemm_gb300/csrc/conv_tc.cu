@@ -92,6 +92,7 @@ struct ConvTcParams {
     int tx_bytes;       // bytes one CTA's copies of a stage deliver
     int stage_bytes;    // kq (S a_box + b_box)
     int nstages_ring;
+    int bar_offset;     // barriers after the operand ring (and after the K split's partial parts)
     int num_stages;     // R0 * R1 * r2_groups * k_groups
     int issuers;        // MMA-issuing threads (1 .. CT_ISSUERS_MAX)
     int nacc;           // TMEM accumulators (issuer i owns i, i + issuers, ...)
@@ -130,7 +131,7 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
     const int SA = p.nstages_ring;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SA * p.stage_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_offset);
     uint64_t* full_bar = bars;             // [SA] both CTAs' copies of the stage landed (even CTA)
     uint64_t* empty_bar = bars + SA;       // [SA] MMAs reading the stage done (both CTAs)
     uint64_t* done_bar = bars + 2 * SA;    // all MMAs done (both CTAs)
@@ -565,7 +566,7 @@ int64_t stages_of_group(int64_t a, int64_t b, int64_t kg, int64_t r2g, int64_t g
 // With tiles for at most a quarter of the SMs, the stage sequence of each tile is split
 // over two pairs (K split, a cluster of four CTAs), so that the pairs fill the SMs.
 int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S, int num_sms,
-                   ConvTcParams* out)
+                   int ks_opt, ConvTcParams* out)
 {
     ConvTcParams p = {};
     if (cin % 16 || cout % 16 || S < 1 || in[3] % S || S * cout > 256) return GEMM_ERR_UNSUPPORTED;
@@ -634,14 +635,18 @@ int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t
     p.nacc = nacc;
     // K split: two pairs per tile (a cluster of four CTAs) when one pair per tile would leave
     // more than half the SMs idle, N is a multiple of 32 (each slot stores half the columns in
-    // 16-column chunks), there are at least two stages, and the partial parts (128 rows x N
-    // fp32 per CTA) fit in the operand ring
+    // 16-column chunks) and there are at least two stages
+    // (ks_opt: 0 choose, 1 one pair per tile, 2 two pairs per tile where the shape allows it)
     const int64_t tiles = (int64_t)p.tiles_per_p0 * p.P[0];
-    p.ks = (num_sms > 0 && 4 * tiles <= num_sms && N % 32 == 0 && p.num_stages >= 2 &&
-            (int64_t)p.nstages_ring * p.stage_bytes >= (int64_t)CT_G * N * 4)
-               ? 2
-               : 1;
+    const bool can_split = N % 32 == 0 && p.num_stages >= 2;
+    if (ks_opt == 2 && !can_split) return GEMM_ERR_UNSUPPORTED;
+    p.ks = ks_opt == 2 ? 2 : ks_opt == 1 ? 1 : (can_split && num_sms > 0 && 4 * tiles <= num_sms) ? 2 : 1;
     if (tiles * p.ks * 2 > 0x7fffffff) return GEMM_ERR_UNSUPPORTED;
+    // the K split's partial parts (128 rows x N fp32) reuse the operand ring's shared memory,
+    // which a short ring may not cover
+    const int64_t ring_bytes = (int64_t)p.nstages_ring * p.stage_bytes;
+    const int64_t part_bytes = p.ks == 2 ? (int64_t)CT_G * N * 4 : 0;
+    p.bar_offset = (int)(ring_bytes > part_bytes ? ring_bytes : part_bytes);
     // accumulator i + issuers j of slot s is written iff issuer i issues more than j MMAs
     // in the slot's stages; issuer i takes MMAs [i n / issuers, (i + 1) n / issuers) of
     // every stage of n MMAs, and n depends on the stage's filter-row group
@@ -671,36 +676,38 @@ int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t
 // them: at 16^4 x 16 -> 32 channels, 5^4 filter, 35.5 us against 37.6 us for two positions
 // without a split, although the stacked zero blocks grow from 1/6 to 3/8 of the products.
 // Else two when the shape allows it, else one.
-int choose_stack(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int num_sms)
+int choose_stack(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int num_sms, int ks_opt)
 {
     ConvTcParams p;
-    if (plan_conv4d_tc(cin, in, cout, k, 4, num_sms, &p) == GEMM_OK) {
+    if (plan_conv4d_tc(cin, in, cout, k, 4, num_sms, ks_opt, &p) == GEMM_OK) {
         const int64_t ctas = (int64_t)2 * p.ks * p.tiles_per_p0 * p.P[0];
         if (p.ks == 2 && ctas <= num_sms && 2 * ctas >= num_sms) return 4;
     }
     for (int S : {2, 1})
-        if (plan_conv4d_tc(cin, in, cout, k, S, num_sms, &p) == GEMM_OK) return S;
+        if (plan_conv4d_tc(cin, in, cout, k, S, num_sms, ks_opt, &p) == GEMM_OK) return S;
     return 0;
 }
 
 }  // namespace
 
-int conv4d_tc_supported(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S, int num_sms)
+int conv4d_tc_supported(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S, int ks_opt,
+                        int num_sms)
 {
     ConvTcParams p;
-    if (S <= 0) S = choose_stack(cin, in, cout, k, num_sms);
-    if (S <= 0 || plan_conv4d_tc(cin, in, cout, k, S, num_sms, &p) != GEMM_OK) return GEMM_ERR_UNSUPPORTED;
+    if (S <= 0) S = choose_stack(cin, in, cout, k, num_sms, ks_opt);
+    if (S <= 0 || plan_conv4d_tc(cin, in, cout, k, S, num_sms, ks_opt, &p) != GEMM_OK) return GEMM_ERR_UNSUPPORTED;
     return GEMM_OK;  // the operands are read straight from the caller's tensors: no workspace
 }
 
 int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void* w, int64_t cout,
-                     const int64_t k[4], float* y, int64_t ldy_cf, bool bf16, int S, int num_sms, int* dev_status,
-                     uint64_t limit_ns, int test_stall, bool programmatic, cudaStream_t stream, int* launches)
+                     const int64_t k[4], float* y, int64_t ldy_cf, bool bf16, int S, int ks_opt, int num_sms,
+                     int* dev_status, uint64_t limit_ns, int test_stall, bool programmatic, cudaStream_t stream,
+                     int* launches)
 {
-    if (S <= 0) S = choose_stack(cin, in, cout, k, num_sms);
+    if (S <= 0) S = choose_stack(cin, in, cout, k, num_sms, ks_opt);
     if (S <= 0) return GEMM_ERR_UNSUPPORTED;
     ConvTcParams p;
-    const int rc = plan_conv4d_tc(cin, in, cout, k, S, num_sms, &p);
+    const int rc = plan_conv4d_tc(cin, in, cout, k, S, num_sms, ks_opt, &p);
     if (rc != GEMM_OK) return rc;
     p.idesc = conv_idesc(bf16, S * p.cout);
     p.y = y;
@@ -710,7 +717,7 @@ int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void
     p.test_stall = test_stall;
     CUtensorMap tmX, tmW;
     if (!encode_conv_maps(&tmX, &tmW, x, w, bf16, p)) return GEMM_ERR_CUDA;
-    const int smem = p.nstages_ring * p.stage_bytes + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+    const int smem = p.bar_offset + 1024 /*barriers*/ + 1024 /*alignment slack*/;
     if (cudaFuncSetAttribute(conv4d_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};

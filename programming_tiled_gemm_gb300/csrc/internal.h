@@ -182,14 +182,17 @@ cudaError_t launch_im2col4d(const float* x, int64_t cin, const int64_t in[4], co
 // Valid 4-D cross-correlation on the tensor cores, channel-last 16-bit operands
 // (conv4d_forward_cl), S output positions stacked along the MMA's N (0 = choose).
 // Workspace bytes it needs (-1 if the shape is not supported).  Returns a gemm_status_t.
-// GEMM_OK if the tensor-core convolution takes the shape (stack S, 0 = choose), else
-// GEMM_ERR_UNSUPPORTED; it needs no workspace.
-int conv4d_tc_supported(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S, int num_sms);
+// GEMM_OK if the tensor-core convolution takes the shape (stack S, 0 = choose; K split
+// ks_opt: 0 choose, 1 none, 2 over two pairs), else GEMM_ERR_UNSUPPORTED; it needs no
+// workspace.
+int conv4d_tc_supported(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int S, int ks_opt,
+                        int num_sms);
 // y channel-last [P][C_out] when ldy_cf == 0, else channel-first (y[o][p] at y + o ldy_cf + p);
 // `programmatic`: launched as a programmatic dependent of the kernel before it in the stream
 int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void* w, int64_t cout,
-                     const int64_t k[4], float* y, int64_t ldy_cf, bool bf16, int S, int num_sms, int* dev_status,
-                     uint64_t limit_ns, int test_stall, bool programmatic, cudaStream_t stream, int* launches);
+                     const int64_t k[4], float* y, int64_t ldy_cf, bool bf16, int S, int ks_opt, int num_sms,
+                     int* dev_status, uint64_t limit_ns, int test_stall, bool programmatic, cudaStream_t stream,
+                     int* launches);
 // 16-bit channel-first to channel-last copies, one launch: x [C][V] -> xc [V][Cp] and
 // w [B][C][T] -> wc [B][T][Cp], channels C .. Cp-1 zero
 cudaError_t launch_to_channel_last(const void* x, int64_t C, int64_t V, void* xc, const void* w, int64_t B,

@@ -106,6 +106,63 @@ def test_stacked_positions_are_exact(lib, stack, cin, cout, ins, ks):
     assert np.array_equal(got, conv_ref(x, w))
 
 
+SPLIT = [  # (stack S, C_in, C_out, input extents, kernel extents) run with and without the K split
+    (4, 16, 32, (16, 16, 16, 16), (5, 5, 5, 5)),   # the workload: 36 tiles, 144 CTAs split
+    (2, 16, 32, (6, 5, 16, 16), (3, 2, 5, 5)),     # a few tiles
+    (4, 32, 32, (3, 4, 9, 12), (2, 2, 3, 3)),      # two 16-channel steps per tap
+    (2, 16, 64, (2, 3, 5, 6), (1, 2, 2, 3)),       # two stages, a ring shorter than the partial parts
+]
+
+
+@pytest.mark.parametrize("stack,cin,cout,ins,ks", SPLIT)
+def test_k_split_over_two_pairs_is_exact_and_matches_one_pair(lib, stack, cin, cout, ins, ks):
+    """GEMM_OPT_CONV_SPLIT 1 (one CTA pair per tile) and 2 (two pairs per tile in a cluster
+    of four, partial tiles added through distributed shared memory): both exact on integer
+    inputs, so both equal the oracle and each other."""
+    import programming_tiled_gemm_gb300 as g
+    x, w = int_operands(cin, cout, ins, ks, seed=3 * stack + cout + sum(ins))
+    ref = conv_ref(x, w)
+    lib.set_option(g.GEMM_OPT_CONV_STACK, stack)
+    try:
+        outs = []
+        for split in (1, 2):
+            lib.set_option(g.GEMM_OPT_CONV_SPLIT, split)
+            outs.append(run_guarded(lib, x, w))
+    finally:
+        lib.set_option(g.GEMM_OPT_CONV_STACK, 0)
+        lib.set_option(g.GEMM_OPT_CONV_SPLIT, 0)
+    assert np.array_equal(outs[0], ref)
+    assert np.array_equal(outs[1], ref)
+
+
+def test_k_split_refusals(lib):
+    """Two pairs per tile need S C_out a multiple of 32 and at least two stages."""
+    import programming_tiled_gemm_gb300 as g
+    dev = torch.device("cuda")
+    h = lib.handle
+    x = torch.zeros((2, 2, 4, 4, 16), dtype=torch.bfloat16, device=dev)
+    w = torch.zeros((16, 1, 1, 2, 2, 16), dtype=torch.bfloat16, device=dev)
+    y = torch.zeros((2, 2, 3, 3, 16), device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    lib.set_option(g.GEMM_OPT_CONV_SPLIT, 2)
+    try:
+        # N = 2 x 16 = 32 but a single stage (one tap triple, one channel step)
+        assert g.conv4d_forward_cl(h, x.data_ptr(), 16, [2, 2, 4, 4], w.data_ptr(), 16, [1, 1, 2, 2], y.data_ptr(),
+                                   g.GEMM_BF16, s) == g.GEMM_ERR_UNSUPPORTED
+        lib.set_option(g.GEMM_OPT_CONV_STACK, 1)  # N = 16: not a multiple of 32
+        w2 = torch.zeros((16, 2, 1, 2, 2, 16), dtype=torch.bfloat16, device=dev)
+        y2 = torch.zeros((1, 2, 3, 3, 16), device=dev)
+        assert g.conv4d_forward_cl(h, x.data_ptr(), 16, [2, 2, 4, 4], w2.data_ptr(), 16, [2, 1, 2, 2], y2.data_ptr(),
+                                   g.GEMM_BF16, s) == g.GEMM_ERR_UNSUPPORTED
+    finally:
+        lib.set_option(g.GEMM_OPT_CONV_SPLIT, 0)
+        lib.set_option(g.GEMM_OPT_CONV_STACK, 0)
+    assert g.gemm_set_option(h, g.GEMM_OPT_CONV_SPLIT, 3) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_set_option(h, g.GEMM_OPT_CONV_SPLIT, -1) == g.GEMM_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert lib.device_status() == g.GEMM_OK
+
+
 def test_integer_inputs_fp16_are_exact(lib):
     x, w = int_operands(32, 32, (4, 4, 9, 11), (2, 3, 3, 4), seed=5, dtype="f16")
     assert np.array_equal(run_guarded(lib, x, w), conv_ref(x, w))
