@@ -189,7 +189,10 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     const int plane = p.I[2] * p.I[3];
     const uint32_t used = p.acc_used[kslot];
     float* const my_part = reinterpret_cast<float*>(smem) + quarter * N * 32;  // K split: [column][lane]
-    bool epi_ok = false;
+    // K split: warps 1..12 (the issuers' and the epilogue's) share the partial parts' traffic,
+    // three warps per TMEM lane quarter, share = (warp - 1) / 4 of the column chunks each
+    const int share = (warp - 1) / 4;
+    bool part_ok = false;  // this warp saw the MMAs complete
     // the accumulators that received MMAs, added in order; 16-column chunks load four
     // accumulators per wait (the 32-column form has no registers to spare for that)
     auto chunk_sum = [&](int c0, int w, auto& acc) {
@@ -401,6 +404,22 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
             }
         }
         __syncwarp();
+        if (p.ks == 2) {
+            // K split: these warps publish their share of the partial part too (waiting,
+            // bounded, for the MMAs; a timeout here is the epilogue's to report)
+            bool ok = mbar_wait_cluster_sleep(smem_u32(done_bar), 0, p.limit_ns, abort_flag, 1000);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                part_ok = true;
+                for (int c0 = 16 * share; c0 < N; c0 += 48) {
+                    float acc[16];
+                    chunk_sum(c0, 16, acc);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) my_part[(c0 + i) * 32 + lane] = acc[i];
+                }
+            }
+        }
     } else {
         // ---------------------------------------------------------------- epilogue (both CTAs)
         bool ok = true;
@@ -419,7 +438,7 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
         if (!ok) aborted = true;
         if (ok) {
             tc_fence_after();
-            epi_ok = true;
+            part_ok = true;
             if (p.ks == 1) {
                 for (int c0 = 0; c0 < N; c0 += 32) {
                     const int w = N - c0 >= 32 ? 32 : 16;
@@ -428,10 +447,11 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
                     chunk_store(c0, w, acc);
                 }
             } else {
-                // K split: this warp's partial part (32 rows x N columns) goes to this CTA's
+                // K split: the partial part (32 rows x N columns per quarter) goes to this CTA's
                 // shared memory (the operand ring, idle once the MMAs are done), laid out
-                // [column][lane] so that a warp's accesses are conflict-free 128-byte rows
-                for (int c0 = 0; c0 < N; c0 += 16) {
+                // [column][lane] so that a warp's accesses are conflict-free 128-byte rows;
+                // this warp's share of the 16-column chunks
+                for (int c0 = 16 * share; c0 < N; c0 += 48) {
                     float acc[16];
                     chunk_sum(c0, 16, acc);
 #pragma unroll
@@ -447,20 +467,21 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
         // slot 0's part + slot 1's part, reading the other slot's through distributed shared
         // memory, and stores y
         cluster_sync_all();
-        if (epi_ok) {
+        if (part_ok) {
+            // this warp's share of the slot's 8-column groups
             const uint32_t peer = crank ^ 2u;  // the same rows in the other slot's pair
             const int c_lo = kslot * (N / 2);
-            for (int c0 = c_lo; c0 < c_lo + N / 2; c0 += 16) {
-                float other[16], acc[16];
+            for (int c0 = c_lo + 8 * share; c0 < c_lo + N / 2; c0 += 24) {
+                float other[8], acc[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
+                for (int i = 0; i < 8; ++i)
                     other[i] = ld_shared_cluster_f32(mapa_shared(smem_u32(my_part + (c0 + i) * 32 + lane), peer));
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     const float own = my_part[(c0 + i) * 32 + lane];
                     acc[i] = kslot == 0 ? __fadd_rn(own, other[i]) : __fadd_rn(other[i], own);
                 }
-                chunk_store(c0, 16, acc);
+                chunk_store(c0, 8, acc);
             }
         }
     }
