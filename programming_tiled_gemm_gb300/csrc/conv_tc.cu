@@ -40,7 +40,8 @@
 //   the kernel ran 43.8 us instead of 37.5 us on the 16^4 x 16, 5^4 x 32 workload.
 // Warp roles (416 threads per CTA): warp 0 = producer (both CTAs), warps 1..8 = MMA issuers
 // (lane 0, even CTA only; warp 1 owns TMEM in both CTAs), warps 9..12 = epilogue (both CTAs,
-// one per 32-lane TMEM quarter).
+// one per 32-lane TMEM quarter).  Once the MMAs are done, warps 1..8 read the accumulators
+// with the epilogue warps: three warps per lane quarter, a third of the columns each.
 //   * accumulation: each issuer's MMAs go round-robin to its share of up to 8 TMEM
 //     accumulators; the tensor core's fp32 accumulator rounds toward zero, so shorter sums
 //     per accumulator keep the error small; the epilogue adds them in fp32
@@ -179,65 +180,49 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     const uint32_t tmem_base = *tmem_holder;
     bool aborted = false;
 
-    // epilogue (warps CT_ISSUERS_MAX + 1 ..): thread = tile row g of this CTA, TMEM lane quarter
-    // `quarter`; columns in chunks of 32 (a last chunk of 16 when N % 32 == 16), or of 16 for
-    // the K split.  The accumulators' parts of a chunk are added in order, then stored as
-    // groups of 8 columns.  Column c = h (S C_out/2) + t' (C_out/2) + o_low is output channel
-    // h C_out/2 + o_low at position ug + S - 1 - t'
+    // Reading the accumulators (warps 1 .. 12, once the MMAs are done): thread = tile row of this
+    // CTA in TMEM lane quarter `quarter`; columns in chunks of 16, the accumulators' parts of a
+    // chunk added in order, then stored as groups of 8 columns.  Column
+    // c = h (S C_out/2) + t' (C_out/2) + o_low is output channel h C_out/2 + o_low at position
+    // ug + S - 1 - t'
     const int quarter = warp & 3;
     const int ug = u0 + ((int)rank * CT_G + quarter * 32 + lane) * p.S;  // this row's first position
     const int plane = p.I[2] * p.I[3];
     const uint32_t used = p.acc_used[kslot];
     float* const my_part = reinterpret_cast<float*>(smem) + quarter * N * 32;  // K split: [column][lane]
-    // K split: warps 1..12 (the issuers' and the epilogue's) share the partial parts' traffic,
-    // three warps per TMEM lane quarter, share = (warp - 1) / 4 of the column chunks each
+    // Warps 1..12 (the issuers' and the epilogue's) read the accumulators once the MMAs are
+    // done: three warps per TMEM lane quarter, warp w takes the 16-column chunks
+    // (w - 1) / 4, + 3, + 6, ...
     const int share = (warp - 1) / 4;
     bool part_ok = false;  // this warp saw the MMAs complete
-    // the accumulators that received MMAs, added in order; 16-column chunks load four
-    // accumulators per wait (the 32-column form has no registers to spare for that)
-    auto chunk_sum = [&](int c0, int w, auto& acc) {
-        constexpr int CW = sizeof(acc) / sizeof(acc[0]);
-        constexpr int BATCH = CW == 16 ? 4 : 1;
+    // a 16-column chunk of this row: the accumulators that received MMAs, added in order, four
+    // TMEM loads per wait
+    auto chunk_sum = [&](int c0, float (&acc)[16]) {
 #pragma unroll
-        for (int i = 0; i < CW; ++i) acc[i] = 0.f;
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0;
-        if (CW == 32 && w == 16) {  // a last chunk of 16 columns, one accumulator at a time
-            for (int a = 0; a < p.nacc; ++a) {
-                if (!((used >> a) & 1)) continue;
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * N), v);
-                tmem_ld_wait();
+        for (int a0 = 0; a0 < p.nacc; a0 += 4) {
+            uint32_t v[4][16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __uint_as_float(v[i]));
-            }
-            return;
-        }
-        for (int a0 = 0; a0 < p.nacc; a0 += BATCH) {
-            uint32_t v[BATCH][CW];
-#pragma unroll
-            for (int b = 0; b < BATCH; ++b) {
+            for (int b = 0; b < 4; ++b) {
                 const int a = a0 + b;
-                if (a >= p.nacc || !((used >> a) & 1)) continue;
-                if constexpr (CW == 32)
-                    tmem_ld_32x32b_x32(lane_base + (uint32_t)(a * N), v[b]);
-                else
-                    tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * N), v[b]);
+                if (a < p.nacc && ((used >> a) & 1)) tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * N), v[b]);
             }
             tmem_ld_wait();
 #pragma unroll
-            for (int b = 0; b < BATCH; ++b) {
+            for (int b = 0; b < 4; ++b) {
                 const int a = a0 + b;
                 if (a >= p.nacc || !((used >> a) & 1)) continue;
 #pragma unroll
-                for (int i = 0; i < CW; ++i) acc[i] = __fadd_rn(acc[i], __uint_as_float(v[b][i]));
+                for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __uint_as_float(v[b][i]));
             }
         }
     };
-    auto chunk_store = [&](int c0, int w, const auto& acc) {
+    // columns c0 .. c0 + CW - 1 of this row to y, in groups of 8 (acc: float[16] or float[8])
+    auto chunk_store = [&](int c0, const auto& acc) {
         constexpr int CW = sizeof(acc) / sizeof(acc[0]);
 #pragma unroll
         for (int j = 0; j < CW; j += 8) {
-            if (j >= w) break;
             const int c = c0 + j;
             const int hh = c / (N / 2), cr = c - hh * (N / 2);
             const int tb = cr / half, o = hh * half + (cr - tb * half);
@@ -255,6 +240,21 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
 #pragma unroll
                     for (int e = 0; e < 8; ++e) ycol[(int64_t)e * p.ldy_cf] = acc[j + e];
                 }
+            }
+        }
+    };
+    // this warp's chunks: stored to y, or with a K split left in shared memory as this CTA's
+    // partial part (the operand ring, idle once the MMAs are done), [column][lane] so that a
+    // warp's accesses are conflict-free 128-byte rows
+    auto epilogue_share = [&]() {
+        for (int c0 = 16 * share; c0 < N; c0 += 48) {
+            float acc[16];
+            chunk_sum(c0, acc);
+            if (p.ks == 1) {
+                chunk_store(c0, acc);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) my_part[(c0 + i) * 32 + lane] = acc[i];
             }
         }
     };
@@ -404,20 +404,15 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
             }
         }
         __syncwarp();
-        if (p.ks == 2) {
-            // K split: these warps publish their share of the partial part too (waiting,
-            // bounded, for the MMAs; a timeout here is the epilogue's to report)
+        {
+            // these warps take their share of the accumulators too (waiting, bounded, for the
+            // MMAs; a timeout here is the epilogue's to report)
             bool ok = mbar_wait_cluster_sleep(smem_u32(done_bar), 0, p.limit_ns, abort_flag, 1000);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
                 part_ok = true;
-                for (int c0 = 16 * share; c0 < N; c0 += 48) {
-                    float acc[16];
-                    chunk_sum(c0, 16, acc);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) my_part[(c0 + i) * 32 + lane] = acc[i];
-                }
+                epilogue_share();
             }
         }
     } else {
@@ -439,25 +434,7 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
         if (ok) {
             tc_fence_after();
             part_ok = true;
-            if (p.ks == 1) {
-                for (int c0 = 0; c0 < N; c0 += 32) {
-                    const int w = N - c0 >= 32 ? 32 : 16;
-                    float acc[32];
-                    chunk_sum(c0, w, acc);
-                    chunk_store(c0, w, acc);
-                }
-            } else {
-                // K split: the partial part (32 rows x N columns per quarter) goes to this CTA's
-                // shared memory (the operand ring, idle once the MMAs are done), laid out
-                // [column][lane] so that a warp's accesses are conflict-free 128-byte rows;
-                // this warp's share of the 16-column chunks
-                for (int c0 = 16 * share; c0 < N; c0 += 48) {
-                    float acc[16];
-                    chunk_sum(c0, 16, acc);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) my_part[(c0 + i) * 32 + lane] = acc[i];
-                }
-            }
+            epilogue_share();
         }
     }
 
@@ -481,7 +458,7 @@ conv4d_tc_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
                     const float own = my_part[(c0 + i) * 32 + lane];
                     acc[i] = kslot == 0 ? __fadd_rn(own, other[i]) : __fadd_rn(other[i], own);
                 }
-                chunk_store(c0, 8, acc);
+                chunk_store(c0, acc);
             }
         }
     }
