@@ -462,18 +462,20 @@ HostStage host_stage_layout(const gemm_host_problem& q, size_t base)
 //   2 to 4 chunks of >= 1024 rows, 4096 and more where M allows, so that each launch
 //   keeps several waves of 256 x 256 tiles (measured at 8192^3: four 2048-row chunks
 //   computed in 0.72 ms, one launch in 0.63 ms).
-//   fp32 is compute-bound: one half of the rows, then three eighths, then one eighth.
-//   The batch's last piece of work then has a small result to bring back.
+//   fp32 is compute-bound: one sixteenth of the rows (the first compute starts after B and
+//   a short slice of A are in), seven sixteenths, three eighths, then one eighth (the
+//   batch's last piece of work then has a small result to bring back).  Measured on the
+//   bf16 8192^3 + fp32 4096^3 batch: 3.45 ms against 3.49 ms with a first chunk of 1/8.
 std::vector<int64_t> host_chunk_rows(const gemm_host_problem& q)
 {
     std::vector<int64_t> rows;
     if (q.M <= 0 || q.N <= 0) return rows;
     auto up256 = [](int64_t v) { return (v + 255) / 256 * 256; };
     if (q.K > 0 && q.dtype == GEMM_F32 && q.M >= 4096) {
-        // 1/8, 3/8, 3/8 and the rest, each rounded up to 256 rows and cut to what is left
-        const int64_t a = up256(q.M / 8), b = up256(q.M * 3 / 8);
+        // 1/16, 7/16, 3/8 and the rest, each rounded up to 256 rows and cut to what is left
+        const int64_t a = up256(q.M / 16), b = up256(q.M * 7 / 16), c = up256(q.M * 3 / 8);
         int64_t left = q.M;
-        for (int64_t want : {a, b, b}) {
+        for (int64_t want : {a, b, c}) {
             const int64_t r = want < left ? want : left;
             if (r > 0) rows.push_back(r);
             left -= r;
