@@ -732,6 +732,16 @@ int launch_conv4d_tc(const void* x, int64_t cin, const int64_t in[4], const void
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 2 : 1;
+    if (p.ks == 2 && ks_opt == 0) {
+        // clusters of four CTAs of ~200 KiB each may not be placeable (a partitioned device):
+        // then one pair per tile, clusters of two
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, conv4d_tc_pair_kernel, &cfg) != cudaSuccess || clusters < 1) {
+            (void)cudaGetLastError();
+            return launch_conv4d_tc(x, cin, in, w, cout, k, y, ldy_cf, bf16, S, 1, num_sms, dev_status, limit_ns,
+                                    test_stall, programmatic, stream, launches);
+        }
+    }
     if (cudaLaunchKernelEx(&cfg, conv4d_tc_pair_kernel, tmX, tmW, p) != cudaSuccess) return GEMM_ERR_CUDA;
     *launches += 1;
     return GEMM_OK;
