@@ -53,7 +53,8 @@
 // in that order, the other slot's read through distributed shared memory; a second cluster
 // barrier keeps every part alive until it has been read.  Both barriers are reached by every
 // thread on every path.  At 16^4 x 16 -> 32 channels, 5^4 filter this lets four positions
-// stack along N (N = 128: MMAs at the full rate) on 144 CTAs: 35.5 us against 37.6 us.
+// stack along N (N = 128: MMAs at the full rate) on 144 CTAs: 29.3 us per call back to back
+// against 35.1 us for two positions and one pair per tile.
 // Every mbarrier wait is bounded (wall clock); on expiry the CTA records an error in the
 // status word, waits (bounded) for its own copies and MMAs in flight, frees its TMEM and
 // returns.
@@ -671,8 +672,9 @@ int plan_conv4d_tc(int64_t cin, const int64_t in[4], int64_t cout, const int64_t
 
 // Positions stacked along N.  Four (N = 4 C_out, MMAs at the full rate from N = 128 on)
 // when that plan, with its K split, fits the SMs in one wave and fills at least half of
-// them: at 16^4 x 16 -> 32 channels, 5^4 filter, 35.5 us against 37.6 us for two positions
-// without a split, although the stacked zero blocks grow from 1/6 to 3/8 of the products.
+// them: at 16^4 x 16 -> 32 channels, 5^4 filter, 29.3 us per call back to back against
+// 35.1 us for two positions without a split, although the stacked zero blocks grow from 1/6
+// to 3/8 of the products.
 // Else two when the shape allows it, else one.
 int choose_stack(int64_t cin, const int64_t in[4], int64_t cout, const int64_t k[4], int num_sms, int ks_opt)
 {
